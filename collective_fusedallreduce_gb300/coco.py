@@ -1,0 +1,221 @@
+"""Thin Python binding of libcoco (include/coco.h): argument marshalling only.
+
+Each ``coco_*`` function here has the name and argument order of the C entry
+point. Distributed tensors are described with ``local``, ``sliced`` and
+``replicated`` ([CoCoNet] "Breaking the Computation and Communication
+Abstraction Barrier in Distributed Machine Learning Workloads", tensor
+layouts) from per-rank ``torch.Tensor`` lists (group-major for several
+groups); PyTorch provides device memory and streams, every computation runs in
+the library's kernels. A failing call raises ``CocoError``.
+
+Importing this module loads ``libcoco.so`` from this package directory and
+raises ``ImportError`` if it has not been built (``__graft_entry__.build()``):
+there is no fallback.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoco.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+MAX_PTRS = 64
+MAX_DIMS = 3
+
+F32, F16, BF16 = 0, 1, 2
+LOCAL, SLICED, REPLICATED = 0, 1, 2
+
+STATUS = {
+    0: "COCO_OK", 1: "COCO_ERR_NULL", 2: "COCO_ERR_SHAPE", 3: "COCO_ERR_DTYPE", 4: "COCO_ERR_LAYOUT",
+    5: "COCO_ERR_ALIGN", 6: "COCO_ERR_ALIAS", 7: "COCO_ERR_UNSUPPORTED", 8: "COCO_ERR_CUDA",
+    9: "COCO_ERR_TIMEOUT", 10: "COCO_ERR_VALUE",
+}
+
+_DTYPES = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+
+class CocoTensor(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int32),
+        ("layout", ctypes.c_int32),
+        ("ndim", ctypes.c_int32),
+        ("slice_dim", ctypes.c_int32),
+        ("shape", ctypes.c_int64 * MAX_DIMS),
+        ("nranks", ctypes.c_int32),
+        ("ngroups", ctypes.c_int32),
+        ("ptr", ctypes.c_void_p * MAX_PTRS),
+    ]
+
+
+class CocoError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        msg = _lib.coco_status_string(status).decode()
+        if status == 8:
+            msg += f" (cudaError {_lib.coco_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+
+
+_P = ctypes.POINTER(CocoTensor)
+_S = ctypes.c_void_p
+for _name, _args in {
+    "coco_fused_allreduce": [_P, ctypes.c_void_p, _P, ctypes.c_float, ctypes.c_uint64, _P, _S],
+    "coco_allreduce": [_P, _P, _S],
+    "coco_reduce_scatter": [_P, _P, _S],
+    "coco_allgather": [_P, _P, _S],
+    "coco_allreduce_rs_ag": [_P, _P, _P, _S],
+    "coco_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
+    "coco_looped_ag_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
+    "coco_looped_einsum_rs": [ctypes.c_char_p, _P, _P, _P, _S],
+    "coco_dropout_keep_mask": [ctypes.c_uint64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p, _S],
+    "coco_device_status": [_S],
+}.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+_lib.coco_status_string.argtypes = [ctypes.c_int]
+_lib.coco_status_string.restype = ctypes.c_char_p
+_lib.coco_last_cuda_error.restype = ctypes.c_int
+_lib.coco_version.restype = ctypes.c_int
+_lib.coco_kernel_launches.restype = ctypes.c_uint64
+
+EXPORTED = [
+    "coco_fused_allreduce", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
+    "coco_einsum", "coco_looped_ag_einsum", "coco_looped_einsum_rs", "coco_dropout_keep_mask",
+    "coco_device_status", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
+]
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def version():
+    return _lib.coco_version()
+
+
+def coco_kernel_launches():
+    return int(_lib.coco_kernel_launches())
+
+
+# ------------------------------------------------------------ tensor specs
+
+
+class Dist:
+    """A distributed tensor: per-rank tensors plus layout (marshalled to coco_tensor)."""
+
+    def __init__(self, layout, tensors, shape, slice_dim=-1, ngroups=1, dtype=None):
+        self.layout = layout
+        self.tensors = list(tensors)
+        self.shape = tuple(int(s) for s in shape)
+        self.slice_dim = slice_dim
+        self.ngroups = ngroups
+        self.nranks = len(self.tensors) // ngroups
+        self.dtype = dtype if dtype is not None else _DTYPES[self.tensors[0].dtype]
+
+    def c(self):
+        t = CocoTensor()
+        t.dtype = self.dtype
+        t.layout = self.layout
+        t.ndim = len(self.shape)
+        t.slice_dim = self.slice_dim
+        for i, s in enumerate(self.shape):
+            t.shape[i] = s
+        t.nranks = self.nranks
+        t.ngroups = self.ngroups
+        for i, x in enumerate(self.tensors):
+            t.ptr[i] = x.data_ptr() if x is not None else None
+        return t
+
+
+def local(tensors, ngroups=1):
+    """Same shape, different values on every rank."""
+    return Dist(LOCAL, tensors, tensors[0].shape, ngroups=ngroups)
+
+
+def replicated(tensors, ngroups=1):
+    """Same values on every rank (a single tensor may be repeated)."""
+    return Dist(REPLICATED, tensors, tensors[0].shape, ngroups=ngroups)
+
+
+def sliced(tensors, dim, ngroups=1):
+    """Rank r holds slice r of a tensor split equally along ``dim``."""
+    nranks = len(tensors) // ngroups
+    shape = list(tensors[0].shape)
+    shape[dim] *= nranks
+    return Dist(SLICED, tensors, shape, slice_dim=dim, ngroups=ngroups)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d.c())
+
+
+def _check(status, where):
+    if status != 0:
+        raise CocoError(status, where)
+
+
+# ------------------------------------------------------------- entry points
+
+
+def coco_fused_allreduce(partials, bias, residual, dropout_p, seed, out, stream=None):
+    bias_ptr = None if bias is None else ctypes.c_void_p(bias.data_ptr())
+    _check(_lib.coco_fused_allreduce(_ref(partials), bias_ptr, _ref(residual), float(dropout_p), int(seed),
+                                     _ref(out), _stream(stream)), "coco_fused_allreduce")
+
+
+def coco_allreduce(inp, out, stream=None):
+    _check(_lib.coco_allreduce(_ref(inp), _ref(out), _stream(stream)), "coco_allreduce")
+
+
+def coco_reduce_scatter(inp, out, stream=None):
+    _check(_lib.coco_reduce_scatter(_ref(inp), _ref(out), _stream(stream)), "coco_reduce_scatter")
+
+
+def coco_allgather(inp, out, stream=None):
+    _check(_lib.coco_allgather(_ref(inp), _ref(out), _stream(stream)), "coco_allgather")
+
+
+def coco_allreduce_rs_ag(inp, scratch, out, stream=None):
+    _check(_lib.coco_allreduce_rs_ag(_ref(inp), _ref(scratch), _ref(out), _stream(stream)), "coco_allreduce_rs_ag")
+
+
+def coco_einsum(spec, lhs, rhs, out, stream=None):
+    _check(_lib.coco_einsum(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), _stream(stream)), "coco_einsum")
+
+
+def coco_looped_ag_einsum(spec, lhs, rhs, out, stream=None):
+    _check(_lib.coco_looped_ag_einsum(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), _stream(stream)),
+           "coco_looped_ag_einsum")
+
+
+def coco_looped_einsum_rs(spec, lhs, rhs, out, stream=None):
+    _check(_lib.coco_looped_einsum_rs(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), _stream(stream)),
+           "coco_looped_einsum_rs")
+
+
+def coco_dropout_keep_mask(seed, dropout_p, first_index, count, mask, stream=None):
+    ptr = None if mask is None else ctypes.c_void_p(mask.data_ptr())
+    _check(_lib.coco_dropout_keep_mask(int(seed), float(dropout_p), int(first_index), int(count), ptr,
+                                       _stream(stream)), "coco_dropout_keep_mask")
+
+
+def coco_device_status(stream=None):
+    _check(_lib.coco_device_status(_stream(stream)), "coco_device_status")
+
+
+def raw_call(name, *args):
+    """Calls a C entry point with already-marshalled ctypes arguments and
+    returns its status code (used by the interface tests)."""
+    return getattr(_lib, name)(*args)

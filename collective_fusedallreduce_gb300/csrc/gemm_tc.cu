@@ -1,0 +1,577 @@
+// Tensor-core GEMM for sm_103a (tcgen05 + TMEM + TMA), driven by a plan of
+// jobs and K-segments so one persistent launch runs every rank's part of a
+// Looped CollectiveEinsum.
+//
+// [Decomp] "Overlap Communication with Dependent Computation via
+// Decomposition in Large Deep Learning Models", §5.1 (Looped
+// CollectiveEinsum, Alg. 1): on one GPU a CollectivePermute of a shard is a
+// read of that shard where it lives, so the loop over shards becomes the
+// order of K-segments (Addition: accumulated in TMEM) or of output jobs
+// (DynamicUpdateSlice: the epilogue's row / column / batch offset).
+//
+// Kernel shape (one CTA per SM, persistent over tiles):
+//   warp 0      TMA producer: A tile [128 x 64] (K-major, 128B swizzle) and
+//               B tile [64 x 256] (N-major: four 64-column boxes, 128B
+//               swizzle) per stage, into a 4-stage mbarrier ring.
+//   warp 1      allocates 512 TMEM columns (two fp32 128x256 accumulators),
+//               one thread issues tcgen05.mma (M=128, N=256, K=16) and
+//               commits stages back to the producer and finished
+//               accumulators to the epilogue.
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, convert, stage a
+//               128-byte-wide swizzled strip in shared memory, then coalesced
+//               16-byte global stores bounded by the job's extent.
+// Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
+// COCO_ERR_TIMEOUT in the error word, raises an abort flag for the other
+// roles, drains its own outstanding copies / MMAs (bounded again), frees TMEM
+// and returns.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace coco {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int B_BOX_BYTES = BK * 64 * 2;         // 8 KB (64 k-rows x 128 B)
+constexpr int B_BYTES = B_BOX_BYTES * (BN / 64);  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
+constexpr int EPI_WARPS = 4;
+constexpr int EPI_STRIP = 32 * 128;                 // per warp: 32 rows x 128 B
+constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * EPI_STRIP;
+constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
+constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int GROUP_M = 16;  // tile rasterisation: 16 m-tiles per group, n-major inside
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+constexpr int MAX_MAPS = 96;
+constexpr int MAX_JOBS = 128;
+constexpr int MAX_SEGS = 256;
+constexpr int MAX_OUTS = 64;
+
+struct TcParams {
+  CUtensorMap maps[MAX_MAPS];
+  Job jobs[MAX_JOBS];
+  Seg segs[MAX_SEGS];
+  OutView outs[MAX_OUTS];
+  int32_t tile_start[MAX_JOBS + 1];
+  int32_t njobs;
+  int32_t total_tiles;
+  uint32_t idesc;
+  int32_t out_dtype;
+  unsigned int* err;
+};
+static_assert(sizeof(TcParams) <= 32000, "kernel parameter block too large");
+
+// ------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait. Returns false on timeout or when another role aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 31) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kTimeoutNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                            int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 or f16 in, fp32 accumulate).
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptors (tcgen05 "matrix descriptor" format:
+// start address >> 4 in bits 0-13, leading byte offset >> 4 in 16-29, stride
+// byte offset >> 4 in 32-45, descriptor version 1 in bits 46-47, swizzle mode
+// in 61-63 with 2 = 128-byte swizzle).
+//
+// A, K-major, 128B swizzle: rows of 128 B (64 elements of K), 8-row groups
+// 1024 B apart (stride byte offset); the K extent of one MMA (32 B) lies
+// inside the swizzle row, so the leading offset is unused. The k-th K=16 slice
+// starts 32*k bytes further.
+__device__ __forceinline__ uint64_t desc_a(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (1ull << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+// B, N-major (MN-major), 128B swizzle: each 64-column box is 64 k-rows of
+// 128 B; 8-row k groups are 1024 B apart (stride byte offset) and 64-column
+// boxes are B_BOX_BYTES apart (leading byte offset). The k-th K=16 slice (two
+// 8-row groups) starts 2048*k bytes further.
+__device__ __forceinline__ uint64_t desc_b(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFF) | (static_cast<uint64_t>(B_BOX_BYTES >> 4) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// ------------------------------------------------------------ tile decode
+
+struct Tile {
+  int job, bb, mt, nt;
+};
+
+__device__ __forceinline__ Tile decode_tile(const TcParams& P, int t) {
+  int lo = 0, hi = P.njobs - 1;
+  while (lo < hi) {  // last job with tile_start <= t
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const Job& J = P.jobs[lo];
+  const int mtiles = (J.m + BM - 1) / BM, ntiles = (J.n + BN - 1) / BN;
+  const int local = t - P.tile_start[lo];
+  const int per_b = mtiles * ntiles;
+  Tile T;
+  T.job = lo;
+  T.bb = local / per_b;
+  const int r = local - T.bb * per_b;
+  const int group = r / (GROUP_M * ntiles);
+  const int first_m = group * GROUP_M;
+  const int gm = min(GROUP_M, mtiles - first_m);
+  const int in_g = r - group * GROUP_M * ntiles;
+  T.mt = first_m + in_g % gm;
+  T.nt = in_g / gm;
+  return T;
+}
+
+// --------------------------------------------------------------- epilogue
+
+__device__ __forceinline__ uint32_t cvt_pair(float a, float b, int out_dtype) {
+  if (out_dtype == COCO_F16) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------ kernel
+
+__global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ TcParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + BAR_OFF;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 8 * NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 8 * NUM_BARS + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 32 * EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicCAS(P.err, 0u, static_cast<unsigned int>(COCO_ERR_TIMEOUT));
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_parity[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) { issued[s] = false; issued_parity[s] = 0; }
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
+        const Tile T = decode_tile(P, t);
+        const Job& J = P.jobs[T.job];
+        for (int si = 0; ok && si < J.nseg; ++si) {
+          const Seg& S = P.segs[J.seg0 + si];
+          const CUtensorMap* ma = &P.maps[S.a];
+          const CUtensorMap* mb = &P.maps[S.b];
+          const int kblocks = (S.klen + BK - 1) / BK;
+          const int arow = S.a_r0 + T.mt * BM, ab = S.a_b0 + T.bb;
+          const int bcol = S.b_c0 + T.nt * BN, bb = S.b_b0 + T.bb;
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+            mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+            tma_load_3d(sa, ma, full_bar(stage), S.a_k0 + kb * BK, arow, ab);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb);
+            issued[stage] = true;
+            issued_parity[stage] = phase;
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+      if (!ok) {  // let copies already in flight land before the CTA exits
+        int dummy = 0;
+        volatile int* never = &dummy;
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) mbar_wait(full_bar(s), issued_parity[s], never);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      bool any_mma = false;
+      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x, ++local) {
+        const Tile T = decode_tile(P, t);
+        const Job& J = P.jobs[T.job];
+        const int acc = local & 1;
+        const uint32_t aph = (local >> 1) & 1;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) { fail(); ok = false; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        uint32_t accumulate = 0;
+        for (int si = 0; ok && si < J.nseg; ++si) {
+          const int kblocks = (P.segs[J.seg0 + si].klen + BK - 1) / BK;
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
+            tc_fence_after();
+            const uint32_t sa = sbase + stage * STAGE_BYTES;
+            const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              umma(d, desc_a(sa + 32 * k), desc_b(sb + 2048 * k), P.idesc, accumulate);
+              accumulate = 1;
+            }
+            any_mma = true;
+            umma_commit(empty_bar(stage));
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if (ok) umma_commit(tfull_bar(acc));
+      }
+      if (!ok && any_mma) {  // wait for the MMAs already issued before TMEM is freed
+        umma_commit(drain_bar);
+        int dummy = 0;
+        volatile int* never = &dummy;
+        mbar_wait(drain_bar, 0, never);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    const uint32_t strip = sbase + EPI_OFF + (warp - 2) * EPI_STRIP;
+    const int out_dt = P.out_dtype;
+    const int esize = out_dt == COCO_F32 ? 4 : 2;
+    const int cols_per_chunk = 128 / esize;  // 32 (fp32) or 64 (16-bit)
+    const int vec_elems = 16 / esize;
+    int local = 0;
+    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++local) {
+      const Tile T = decode_tile(P, t);
+      const Job& J = P.jobs[T.job];
+      const OutView& O = P.outs[J.out];
+      const int acc = local & 1;
+      const uint32_t aph = (local >> 1) & 1;
+      // all lanes must agree before the warp-collective TMEM loads
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag));
+      if (!ready) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      const int row0 = T.mt * BM + quarter * 32;  // job-relative row of this warp's lane 0
+      const int64_t obatch = static_cast<int64_t>(J.o_b0 + T.bb) * O.bstride;
+      for (int c0 = 0; c0 < BN; c0 += cols_per_chunk) {
+        // TMEM -> registers -> swizzled strip (row = lane, 8 chunks of 16 B)
+        uint32_t r[32];
+        if (out_dt == COCO_F32) {
+          tmem_ld32(tbase + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
+                         r[4 * c + 3]);
+        } else {
+          uint32_t r2[32];
+          tmem_ld32(tbase + c0, r);
+          tmem_ld32(tbase + c0 + 32, r2);
+          tmem_ld_wait();
+          uint32_t p[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            p[i] = cvt_pair(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), out_dt);
+            p[16 + i] = cvt_pair(__uint_as_float(r2[2 * i]), __uint_as_float(r2[2 * i + 1]), out_dt);
+          }
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2],
+                         p[4 * c + 3]);
+        }
+        __syncwarp();
+        // strip -> global: 8 lanes per 128-byte row segment, 4 rows per pass
+        const int ch = lane & 7;
+        const int col = T.nt * BN + c0 + ch * vec_elems;  // job-relative column
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = it * 4 + (lane >> 3);
+          const int row = row0 + rr;
+          const uint4 v = ld_shared_v4(strip + rr * 128 + ((ch ^ (rr & 7)) << 4));
+          if (row < J.m && col < J.n) {
+            const int64_t off = obatch + static_cast<int64_t>(J.o_r0 + row) * O.ld + (J.o_c0 + col);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(O.ptr) + off * esize);
+            *dst = v;
+          }
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A operand: [nb][rows][cols=K], box {64 k, 128 rows}. B operand: [nb][rows=K][cols=N], box {64 n, 64 k}.
+bool encode_view(CUtensorMap* map, const View& v, int dtype, bool is_a) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int es = 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(v.cols), static_cast<cuuint64_t>(v.rows),
+                        static_cast<cuuint64_t>(v.nb)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(v.ld) * es, static_cast<cuuint64_t>(v.bstride) * es};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(is_a ? BM : BK), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      dtype == COCO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, dt, 3, const_cast<void*>(v.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool smem_configured[64] = {false};
+
+}  // namespace
+
+static __device__ unsigned int g_gemm_error = 0;
+
+unsigned int* gemm_error_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_gemm_error) != cudaSuccess) return nullptr;
+  return static_cast<unsigned int*>(p);
+}
+
+// Splits the plan into launches that fit the parameter block, remapping view,
+// segment and output indices, then launches each.
+cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* err_word) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !smem_configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    smem_configured[dev] = true;
+  }
+  // A-views are used with the A box and B-views with the B box; a view used
+  // on both sides gets two maps.
+  TcParams* P = new TcParams;
+  cudaError_t status = cudaSuccess;
+  size_t j = 0;
+  const int fmt = plan.in_dtype == COCO_BF16 ? 1 : 0;
+  const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
+                         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+  while (j < plan.jobs.size() && status == cudaSuccess) {
+    memset(P, 0, sizeof(TcParams));
+    std::vector<int> amap(plan.views.size(), -1), bmap(plan.views.size(), -1), omap(plan.outs.size(), -1);
+    int nmaps = 0, nsegs = 0, nouts = 0, njobs = 0, tiles = 0;
+    while (j < plan.jobs.size() && njobs < MAX_JOBS) {
+      const Job& J = plan.jobs[j];
+      // resources this job needs beyond what the launch already has
+      int need_maps = 0;
+      for (int k = 0; k < J.nseg; ++k) {
+        const Seg& S = plan.segs[J.seg0 + k];
+        need_maps += amap[S.a] < 0;
+        need_maps += bmap[S.b] < 0;
+      }
+      const int need_out = omap[J.out] < 0;
+      if (nmaps + need_maps > MAX_MAPS || nsegs + J.nseg > MAX_SEGS || nouts + need_out > MAX_OUTS) break;
+      Job nj = J;
+      nj.seg0 = static_cast<int16_t>(nsegs);
+      for (int k = 0; k < J.nseg; ++k) {
+        Seg S = plan.segs[J.seg0 + k];
+        if (amap[S.a] < 0) {
+          if (!encode_view(&P->maps[nmaps], plan.views[S.a], plan.in_dtype, true)) { status = cudaErrorInvalidValue; break; }
+          amap[S.a] = nmaps++;
+        }
+        if (bmap[S.b] < 0) {
+          if (!encode_view(&P->maps[nmaps], plan.views[S.b], plan.in_dtype, false)) { status = cudaErrorInvalidValue; break; }
+          bmap[S.b] = nmaps++;
+        }
+        S.a = static_cast<int16_t>(amap[S.a]);
+        S.b = static_cast<int16_t>(bmap[S.b]);
+        P->segs[nsegs++] = S;
+      }
+      if (status != cudaSuccess) break;
+      if (omap[J.out] < 0) {
+        P->outs[nouts] = plan.outs[J.out];
+        omap[J.out] = nouts++;
+      }
+      nj.out = omap[J.out];
+      P->jobs[njobs] = nj;
+      P->tile_start[njobs] = tiles;
+      tiles += J.nb * ((J.m + BM - 1) / BM) * ((J.n + BN - 1) / BN);
+      ++njobs;
+      ++j;
+    }
+    if (status != cudaSuccess) break;
+    if (njobs == 0) { status = cudaErrorInvalidValue; break; }  // a single job exceeds the limits
+    P->tile_start[njobs] = tiles;
+    P->njobs = njobs;
+    P->total_tiles = tiles;
+    P->idesc = idesc;
+    P->out_dtype = plan.out_dtype;
+    P->err = err_word;
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(*P);
+    count_launch();
+    status = cudaGetLastError();
+  }
+  delete P;
+  return status;
+}
+
+}  // namespace coco

@@ -1,0 +1,432 @@
+// N-way reduction kernels over N logical ranks in one GPU's memory:
+// FusedAllReduce (sum + bias + counter-hash dropout + residual in registers),
+// plain AllReduce, ReduceScatter and AllGather.
+//
+// [CoCoNet] "Breaking the Computation and Communication Abstraction Barrier in
+// Distributed Machine Learning Workloads", §5.2 (Fused Collective
+// Communication) and Fig. 3; [Decomp] "Overlap Communication with Dependent
+// Computation via Decomposition in Large Deep Learning Models", §2.1.
+//
+// Design (HBM-bound streaming): every thread moves 16-byte vectors; a block
+// handles U vectors per thread per iteration, laid out so each warp access is
+// a fully coalesced 512-byte run; all N loads of an iteration are issued
+// before the first add so ~N*U*16 bytes are in flight per thread; sums run in
+// fp32 in rank order 0..N-1 and each output is rounded once. Grids are a
+// multiple of the SM count and stride over the data.
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace coco {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 2;
+
+// ---------------------------------------------------------------- vectors
+
+template <typename T>
+struct V16;
+
+template <>
+struct V16<float> {
+  static constexpr int N = 4;
+  __device__ static void load(uint4 r, float* f) {
+    f[0] = __uint_as_float(r.x); f[1] = __uint_as_float(r.y);
+    f[2] = __uint_as_float(r.z); f[3] = __uint_as_float(r.w);
+  }
+  __device__ static uint4 store(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_b2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <>
+struct V16<__half> {
+  static constexpr int N = 8;
+  __device__ static void load(uint4 r, float* f) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = p.x; f[2 * i + 1] = p.y;
+    }
+  }
+  __device__ static uint4 store(const float* f) {
+    return make_uint4(pack_h2(f[0], f[1]), pack_h2(f[2], f[3]), pack_h2(f[4], f[5]), pack_h2(f[6], f[7]));
+  }
+};
+
+template <>
+struct V16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(uint4 r, float* f) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[2 * i] = p.x; f[2 * i + 1] = p.y;
+    }
+  }
+  __device__ static uint4 store(const float* f) {
+    return make_uint4(pack_b2(f[0], f[1]), pack_b2(f[2], f[3]), pack_b2(f[4], f[5]), pack_b2(f[6], f[7]));
+  }
+};
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_vec(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// -------------------------------------------------------------- dropout hash
+//
+// Element e is kept iff (splitmix64 output number e+1 from state `seed`) >> 40
+// is below the threshold. The generator (Steele, Lea and Flood, OOPSLA 2014)
+// advances its state by the golden gamma and outputs a two-multiply mix of it.
+// Only the top 24 bits are compared, and the mix's final xor-shift by 31 does
+// not change bits 40..63, so it is skipped here.
+
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+constexpr uint64_t kMix1 = 0xBF58476D1CE4E5B9ull;
+constexpr uint64_t kMix2 = 0x94D049BB133111EBull;
+
+__device__ __forceinline__ bool keep_state(uint64_t z, uint32_t threshold) {
+  z = (z ^ (z >> 30)) * kMix1;
+  z = (z ^ (z >> 27)) * kMix2;
+  return static_cast<uint32_t>(z >> 40) < threshold;
+}
+
+// ----------------------------------------------------------- FusedAllReduce
+
+struct FarArgs {
+  ReduceTables t;
+  int32_t nranks;
+  int64_t nvec;          // vectors per rank
+  const void* bias;      // nullptr = none
+  int32_t bias_vecs;     // H / VEC
+  uint32_t threshold;
+  float scale;
+  uint64_t seed;
+};
+
+// NR: compile-time rank count (0 = runtime, processed 8 at a time).
+template <typename T, int NR, bool DROP>
+__global__ void __launch_bounds__(kThreads) k_fused_allreduce(const __grid_constant__ FarArgs a) {
+  using V = V16<T>;
+  constexpr int VE = V::N;
+  const int g = blockIdx.y;
+  const int nr = NR ? NR : a.nranks;
+  const void* const* in = a.t.in + g * a.nranks;
+  void* const* out = a.t.out + g * a.nranks;
+  const int nout = a.t.nout[g];
+  const char* res = static_cast<const char*>(a.t.residual[g]);
+  const char* bias = static_cast<const char*>(a.bias);
+
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * kUnroll;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * kUnroll + threadIdx.x; base < a.nvec;
+       base += step) {
+    float acc[kUnroll][VE];
+    int64_t vi[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) vi[u] = base + u * kThreads;
+
+    if constexpr (NR > 0) {
+      uint4 raw[kUnroll][NR];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+          if (vi[u] < a.nvec) raw[u][r] = ld_stream(static_cast<const char*>(in[r]) + vi[u] * 16);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (vi[u] >= a.nvec) continue;
+        V::load(raw[u][0], acc[u]);
+#pragma unroll
+        for (int r = 1; r < NR; ++r) {
+          float f[VE];
+          V::load(raw[u][r], f);
+#pragma unroll
+          for (int j = 0; j < VE; ++j) acc[u][j] += f[j];
+        }
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (vi[u] >= a.nvec) continue;
+        V::load(ld_stream(static_cast<const char*>(in[0]) + vi[u] * 16), acc[u]);
+        for (int r0 = 1; r0 < nr; r0 += 8) {
+          uint4 raw[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            if (r0 + r < nr) raw[r] = ld_stream(static_cast<const char*>(in[r0 + r]) + vi[u] * 16);
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            if (r0 + r < nr) {
+              float f[VE];
+              V::load(raw[r], f);
+#pragma unroll
+              for (int j = 0; j < VE; ++j) acc[u][j] += f[j];
+            }
+          }
+        }
+      }
+    }
+
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t v = vi[u];
+      if (v >= a.nvec) continue;
+      if (bias) {
+        float f[VE];
+        const int64_t bv = a.nvec < (int64_t(1) << 31)
+                               ? static_cast<int64_t>(static_cast<uint32_t>(v) % static_cast<uint32_t>(a.bias_vecs))
+                               : v % a.bias_vecs;
+        V::load(*reinterpret_cast<const uint4*>(bias + bv * 16), f);
+#pragma unroll
+        for (int j = 0; j < VE; ++j) acc[u][j] += f[j];
+      }
+      if constexpr (DROP) {
+        // state of element e = v*VE + j is seed + (e + 1) * gamma
+        uint64_t z = a.seed + (static_cast<uint64_t>(v) * VE + 1ull) * kGamma;
+#pragma unroll
+        for (int j = 0; j < VE; ++j) {
+          acc[u][j] = keep_state(z, a.threshold) ? acc[u][j] * a.scale : 0.0f;
+          z += kGamma;
+        }
+      }
+      if (res) {
+        float f[VE];
+        V::load(ld_stream(res + v * 16), f);
+#pragma unroll
+        for (int j = 0; j < VE; ++j) acc[u][j] += f[j];
+      }
+      const uint4 o = V::store(acc[u]);
+      for (int q = 0; q < nout; ++q) st_vec(static_cast<char*>(out[q]) + v * 16, o);
+    }
+  }
+}
+
+// ------------------------------------------------------------ ReduceScatter
+//
+// Grid y = group * nranks + r: block row (g, r) produces rank r's slice,
+// out_r[o, c] = sum_q in_q[o, r*chunk + c] over the [outer, chunk] view of
+// the slice (chunk = slice length * inner, in vectors).
+
+struct SliceArgs {
+  ReduceTables t;
+  int32_t nranks;
+  int64_t outer;
+  int64_t chunk_vecs;   // contiguous vectors of one slice per outer index
+  int64_t row_vecs;     // vectors of one whole outer row (mid * inner / VEC)
+};
+
+template <typename T, int NR>
+__global__ void __launch_bounds__(kThreads) k_reduce_scatter(const __grid_constant__ SliceArgs a) {
+  using V = V16<T>;
+  constexpr int VE = V::N;
+  const int gr = blockIdx.y;
+  const int g = gr / a.nranks, r = gr % a.nranks;
+  const int nr = NR ? NR : a.nranks;
+  const void* const* in = a.t.in + g * a.nranks;
+  char* out = static_cast<char*>(a.t.out[gr]);
+  const int64_t total = a.outer * a.chunk_vecs;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < total; i += step) {
+    int64_t src = r * a.chunk_vecs + i;
+    if (a.outer > 1) {
+      const int64_t o = i / a.chunk_vecs;
+      src = o * a.row_vecs + r * a.chunk_vecs + (i - o * a.chunk_vecs);
+    }
+    float acc[VE];
+    if constexpr (NR > 0) {
+      uint4 raw[NR];
+#pragma unroll
+      for (int q = 0; q < NR; ++q) raw[q] = ld_stream(static_cast<const char*>(in[q]) + src * 16);
+      V::load(raw[0], acc);
+#pragma unroll
+      for (int q = 1; q < NR; ++q) {
+        float f[VE];
+        V::load(raw[q], f);
+#pragma unroll
+        for (int j = 0; j < VE; ++j) acc[j] += f[j];
+      }
+    } else {
+      V::load(ld_stream(static_cast<const char*>(in[0]) + src * 16), acc);
+      for (int q = 1; q < nr; ++q) {
+        float f[VE];
+        V::load(ld_stream(static_cast<const char*>(in[q]) + src * 16), f);
+#pragma unroll
+        for (int j = 0; j < VE; ++j) acc[j] += f[j];
+      }
+    }
+    st_vec(out + i * 16, V::store(acc));
+  }
+}
+
+// ---------------------------------------------------------------- AllGather
+//
+// Grid y = group * nranks + s: block row (g, s) copies shard s into slot s of
+// every distinct destination of group g. A bit-exact 16-byte copy.
+
+__global__ void __launch_bounds__(kThreads) k_allgather(const __grid_constant__ SliceArgs a) {
+  const int gs = blockIdx.y;
+  const int g = gs / a.nranks, s = gs % a.nranks;
+  const char* in = static_cast<const char*>(a.t.in[gs]);
+  void* const* out = a.t.out + g * a.nranks;
+  const int nout = a.t.nout[g];
+  const int64_t total = a.outer * a.chunk_vecs;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * kUnroll;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * kUnroll + threadIdx.x; base < total;
+       base += step) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (base + u * kThreads < total) v[u] = ld_stream(in + (base + u * kThreads) * 16);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t i = base + u * kThreads;
+      if (i >= total) continue;
+      int64_t dst = s * a.chunk_vecs + i;
+      if (a.outer > 1) {
+        const int64_t o = i / a.chunk_vecs;
+        dst = o * a.row_vecs + s * a.chunk_vecs + (i - o * a.chunk_vecs);
+      }
+      for (int q = 0; q < nout; ++q) st_vec(static_cast<char*>(out[q]) + dst * 16, v[u]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ mask
+
+__global__ void k_keep_mask(uint64_t seed, uint32_t threshold, uint64_t first, uint64_t count, uint8_t* mask) {
+  const uint64_t step = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count; i += step) {
+    const uint64_t e = first + i;
+    mask[i] = keep_state(seed + (e + 1ull) * kGamma, threshold) ? 1 : 0;
+  }
+}
+
+// --------------------------------------------------------------- launchers
+
+int grid_for(int64_t work_items, int per_block) {
+  const int64_t want = (work_items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;  // 8 blocks of 256 threads fill an SM
+  int64_t g = want < cap ? want : cap;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+template <typename T, bool DROP>
+cudaError_t far_typed(const FarArgs& a, int nranks, int ngroups, cudaStream_t s) {
+  dim3 grid(grid_for(a.nvec, kThreads * kUnroll), ngroups);
+  switch (nranks) {
+    case 1: k_fused_allreduce<T, 1, DROP><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: k_fused_allreduce<T, 2, DROP><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: k_fused_allreduce<T, 4, DROP><<<grid, kThreads, 0, s>>>(a); break;
+    case 8: k_fused_allreduce<T, 8, DROP><<<grid, kThreads, 0, s>>>(a); break;
+    default: k_fused_allreduce<T, 0, DROP><<<grid, kThreads, 0, s>>>(a); break;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t rs_typed(const SliceArgs& a, int nranks, int ngroups, cudaStream_t s) {
+  dim3 grid(grid_for(a.outer * a.chunk_vecs, kThreads), ngroups * nranks);
+  switch (nranks) {
+    case 1: k_reduce_scatter<T, 1><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: k_reduce_scatter<T, 2><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: k_reduce_scatter<T, 4><<<grid, kThreads, 0, s>>>(a); break;
+    case 8: k_reduce_scatter<T, 8><<<grid, kThreads, 0, s>>>(a); break;
+    default: k_reduce_scatter<T, 0><<<grid, kThreads, 0, s>>>(a); break;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+cudaError_t launch_fused_allreduce(const FarLaunch& L, cudaStream_t s) {
+  FarArgs a;
+  a.t = L.t;
+  a.nranks = L.nranks;
+  const int ve = 16 / dtype_size(L.dtype);
+  a.nvec = L.numel / ve;
+  a.bias = L.bias;
+  a.bias_vecs = static_cast<int32_t>(L.bias ? L.bias_len / ve : 1);
+  a.threshold = L.keep_threshold;
+  a.scale = L.scale;
+  a.seed = L.seed;
+  switch (L.dtype) {
+    case COCO_F32:
+      return L.dropout ? far_typed<float, true>(a, L.nranks, L.ngroups, s) : far_typed<float, false>(a, L.nranks, L.ngroups, s);
+    case COCO_F16:
+      return L.dropout ? far_typed<__half, true>(a, L.nranks, L.ngroups, s) : far_typed<__half, false>(a, L.nranks, L.ngroups, s);
+    default:
+      return L.dropout ? far_typed<__nv_bfloat16, true>(a, L.nranks, L.ngroups, s)
+                       : far_typed<__nv_bfloat16, false>(a, L.nranks, L.ngroups, s);
+  }
+}
+
+static SliceArgs slice_args(const SliceLaunch& L) {
+  SliceArgs a;
+  a.t = L.t;
+  a.nranks = L.nranks;
+  const int ve = 16 / dtype_size(L.dtype);
+  a.outer = L.outer;
+  a.chunk_vecs = (L.mid / L.nranks) * L.inner / ve;
+  a.row_vecs = L.mid * L.inner / ve;
+  return a;
+}
+
+cudaError_t launch_reduce_scatter(const SliceLaunch& L, cudaStream_t s) {
+  const SliceArgs a = slice_args(L);
+  switch (L.dtype) {
+    case COCO_F32: return rs_typed<float>(a, L.nranks, L.ngroups, s);
+    case COCO_F16: return rs_typed<__half>(a, L.nranks, L.ngroups, s);
+    default: return rs_typed<__nv_bfloat16>(a, L.nranks, L.ngroups, s);
+  }
+}
+
+cudaError_t launch_allgather(const SliceLaunch& L, cudaStream_t s) {
+  const SliceArgs a = slice_args(L);
+  dim3 grid(grid_for(a.outer * a.chunk_vecs, kThreads * kUnroll), L.ngroups * L.nranks);
+  k_allgather<<<grid, kThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_keep_mask(uint64_t seed, uint32_t threshold, uint64_t first, uint64_t count, uint8_t* mask,
+                             cudaStream_t s) {
+  k_keep_mask<<<grid_for(static_cast<int64_t>(count), 256), 256, 0, s>>>(seed, threshold, first, count, mask);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace coco

@@ -1,0 +1,245 @@
+/*
+ * coco.h -- C interface of libcoco: collectives fused with, and decomposed
+ * around, their dependent computation, for N logical ranks whose buffers all
+ * live in the memory of one GPU (sm_103a).
+ *
+ * Sources (cited by title and section):
+ *   [CoCoNet] "Breaking the Computation and Communication Abstraction Barrier
+ *             in Distributed Machine Learning Workloads" (ASPLOS '22).
+ *   [Decomp]  "Overlap Communication with Dependent Computation via
+ *             Decomposition in Large Deep Learning Models" (ASPLOS '23).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Tensors. A coco_tensor describes one distributed tensor in [CoCoNet]'s
+ * layout terms (the tensor-layout description accompanying its Fig. 3):
+ *   COCO_SLICED     equally split along `slice_dim` over the ranks; rank r
+ *                   holds slice r. `shape` is the GLOBAL shape and
+ *                   shape[slice_dim] must divide by `nranks`.
+ *   COCO_REPLICATED the same values on every rank. `shape` is the per-rank
+ *                   shape. An input is read from ptr[g*nranks + 0] only; an
+ *                   output is written to every DISTINCT pointer of the group
+ *                   (pass one pointer nranks times to get one copy).
+ *   COCO_LOCAL      same shape, different values on every rank. `shape` is the
+ *                   per-rank shape.
+ * `ngroups` independent groups of `nranks` ranks each (the subgroups of a 2-D
+ * device mesh, [Decomp] §2.2 Fig. 3) share one call; pointers are group-major:
+ * ptr[g*nranks + r] is rank r of group g.
+ *
+ * Memory. Every pointer is a device pointer owned by the caller; each rank's
+ * buffer is dense and row-major. The library allocates no device memory.
+ * Device pointers must be 16-byte aligned and the innermost per-rank
+ * dimension a multiple of 8 elements, else COCO_ERR_ALIGN.
+ *
+ * Streams. `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * Every call validates its arguments on the host, returns an error before any
+ * CUDA call if they are invalid, and otherwise enqueues its kernels on
+ * `stream` and returns without synchronising. All N ranks of all groups are
+ * processed by the one call.
+ *
+ * Aliasing. An output may not overlap any input, except where an entry point
+ * says otherwise; violations return COCO_ERR_ALIAS.
+ *
+ * Errors. The return value is the only error channel. COCO_ERR_CUDA means a
+ * launch failed (the CUDA error is kept: coco_last_cuda_error()). Device-side
+ * waits are bounded; a wait that gives up records COCO_ERR_TIMEOUT, which
+ * coco_device_status() reports.
+ *
+ * Empty tensors (a zero in any extent) are valid: the call returns COCO_OK
+ * and launches nothing.
+ */
+#ifndef COCO_H_
+#define COCO_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  COCO_OK = 0,
+  COCO_ERR_NULL = 1,        /* a required pointer is NULL */
+  COCO_ERR_SHAPE = 2,       /* shapes or rank counts disagree, or a slice is uneven */
+  COCO_ERR_DTYPE = 3,       /* unknown dtype, or operand dtypes disagree */
+  COCO_ERR_LAYOUT = 4,      /* an operand has a layout the operation does not take */
+  COCO_ERR_ALIGN = 5,       /* pointer not 16-byte aligned, or inner dim not a multiple of 8 */
+  COCO_ERR_ALIAS = 6,       /* an output overlaps an input or another output */
+  COCO_ERR_UNSUPPORTED = 7, /* valid request outside what this build implements */
+  COCO_ERR_CUDA = 8,        /* a CUDA runtime call or kernel launch failed */
+  COCO_ERR_TIMEOUT = 9,     /* a bounded device-side wait gave up */
+  COCO_ERR_VALUE = 10       /* a scalar argument is out of range (e.g. dropout p) */
+} coco_status;
+
+typedef enum { COCO_F32 = 0, COCO_F16 = 1, COCO_BF16 = 2 } coco_dtype;
+
+typedef enum { COCO_LOCAL = 0, COCO_SLICED = 1, COCO_REPLICATED = 2 } coco_layout;
+
+#define COCO_MAX_PTRS 64 /* ngroups * nranks <= COCO_MAX_PTRS */
+#define COCO_MAX_DIMS 3
+
+typedef struct {
+  int32_t dtype;                 /* coco_dtype */
+  int32_t layout;                /* coco_layout */
+  int32_t ndim;                  /* 1..COCO_MAX_DIMS */
+  int32_t slice_dim;             /* COCO_SLICED only: the sliced dimension */
+  int64_t shape[COCO_MAX_DIMS];  /* global shape if SLICED, per-rank shape otherwise */
+  int32_t nranks;                /* ranks per group, 1..COCO_MAX_PTRS */
+  int32_t ngroups;               /* independent groups, >= 1 */
+  void* ptr[COCO_MAX_PTRS];      /* device pointers, ptr[g*nranks + r] */
+} coco_tensor;
+
+/* ------------------------------------------------------------------ fused */
+
+/*
+ * FusedAllReduce ([CoCoNet] §5.2 and the AllReduce Fuse transformation;
+ * the computation of its Fig. 3, lines 9-13):
+ *
+ *   out_q[e] = dropout( sum_{r=0}^{N-1} partials_r[e] + bias[e mod H] ) + residual[e]
+ *
+ * for every rank q of every group, with the sum, bias, dropout scale and
+ * residual in fp32 registers and one rounding to the output type at the
+ * store; the summed value is never written to memory.
+ *
+ *   partials  LOCAL, dtype T in {F32, F16, BF16}, any per-rank shape S.
+ *   bias      device pointer to H = S[ndim-1] elements of T, or NULL.
+ *   residual  REPLICATED, dtype T, shape S, or NULL (read from rank 0's pointer).
+ *   dropout_p probability of dropping, in [0, 1]; 0 disables dropout.
+ *   seed      dropout seed. Element e (0-based row-major index inside one
+ *             rank's tensor, the same on every rank and group) is kept iff
+ *             (splitmix64(seed, e) >> 40) < floor((1 - p) * 2^24), where
+ *             splitmix64(seed, e) is the (e+1)-th output of SplitMix64
+ *             started at state `seed`; kept values are multiplied by
+ *             (float)(1 / (1 - p)) and dropped ones become 0 before the
+ *             residual is added. Bit-exact: see coco_dropout_keep_mask.
+ *   out       REPLICATED, dtype T, shape S. out_q may equal partials_q or the
+ *             residual pointer exactly (in place); any other overlap is
+ *             COCO_ERR_ALIAS.
+ */
+coco_status coco_fused_allreduce(const coco_tensor* partials, const void* bias,
+                                 const coco_tensor* residual, float dropout_p, uint64_t seed,
+                                 const coco_tensor* out, void* stream);
+
+/*
+ * Plain AllReduce ([Decomp] §2.1): out_q = sum_r in_r (fp32 sum in rank order
+ * 0..N-1, one rounding), for every rank q. in LOCAL, out REPLICATED, same
+ * dtype and shape. In place (out_q == in_q exactly) is allowed.
+ */
+coco_status coco_allreduce(const coco_tensor* in, const coco_tensor* out, void* stream);
+
+/*
+ * ReduceScatter ([Decomp] §2.1): rank r receives slice r (along
+ * out->slice_dim) of sum_q in_q, summed in fp32 in rank order 0..N-1.
+ * in LOCAL with per-rank shape S; out SLICED with global shape S.
+ */
+coco_status coco_reduce_scatter(const coco_tensor* in, const coco_tensor* out, void* stream);
+
+/*
+ * AllGather ([Decomp] §2.1): every rank receives the concatenation, in
+ * partition-ID order along in->slice_dim, of all ranks' slices. in SLICED with
+ * global shape S; out REPLICATED with shape S. A bit-exact copy.
+ */
+coco_status coco_allgather(const coco_tensor* in, const coco_tensor* out, void* stream);
+
+/*
+ * AllReduce Split RS-AG ([CoCoNet], split transformation): a ReduceScatter of
+ * `in` into `scratch` (the sliced intermediate) followed by an AllGather of
+ * `scratch` into `out`. in LOCAL shape S; scratch SLICED global shape S (the
+ * caller's memory; slice_dim chooses the split); out REPLICATED shape S.
+ * Bit-identical to coco_allreduce (both sum in fp32 in rank order).
+ */
+coco_status coco_allreduce_rs_ag(const coco_tensor* in, const coco_tensor* scratch,
+                                 const coco_tensor* out, void* stream);
+
+/* ---------------------------------------------------------------- einsums */
+
+/*
+ * Supported specs: "mk,kn->mn" (2-D operands) and "bmk,bkn->bmn" (3-D).
+ * Operand storage: lhs row-major [.., m, k], rhs row-major [.., k, n], out
+ * row-major [.., m, n]. lhs and rhs share a dtype; BF16 and F16 run on the
+ * tensor cores with fp32 accumulation; F32 runs on fp32 FMA units. The output
+ * dtype is out->dtype (F32, F16 or BF16), rounded once from the fp32
+ * accumulator.
+ */
+
+/*
+ * Local MatMul ([CoCoNet] Fig. 3 line 7 and its layout rule: MatMul of two
+ * tensors sliced on the contracting dimension yields a local tensor):
+ * out_r = lhs_r @ rhs_r for every rank. lhs: LOCAL, or SLICED on k; rhs:
+ * LOCAL or REPLICATED, or SLICED on k; out: LOCAL (per-rank shape).
+ */
+coco_status coco_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                        const coco_tensor* out, void* stream);
+
+/*
+ * Looped AllGather-Einsum ([Decomp] §4 Fig. 4 and §5.1, Alg. 1): exactly one
+ * operand is SLICED (the looped operand); the other is LOCAL or REPLICATED
+ * (the local operand). Rank r computes, for i = 0..N-1 in this order, the
+ * partial einsum with shard s = (r + i) mod N of the looped operand (the
+ * shard it holds after i CollectivePermutes along {j -> j-1}), and updates
+ * the result:
+ *   looped operand sliced on a non-contracting dim (m of lhs / n of rhs):
+ *       case 1, DynamicUpdateSlice of the shard's rows / columns;
+ *   sliced on the contracting dim k: case 2, the local operand is
+ *       DynamicSliced along k and the Update is an Addition (accumulated in
+ *       fp32 across all N steps, stored once);
+ *   sliced on the batch dim b: case 3, the local operand is DynamicSliced
+ *       along b and the result DynamicUpdateSliced along b.
+ * out: LOCAL with the full (gathered) per-rank result shape, or REPLICATED if
+ * the local operand is REPLICATED.
+ */
+coco_status coco_looped_ag_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                  const coco_tensor* out, void* stream);
+
+/*
+ * Looped Einsum-ReduceScatter ([Decomp] §4 Fig. 5 and §5.1): lhs and rhs are
+ * both SLICED on the contracting dimension k (so each rank's product is a
+ * local partial sum); out is SLICED on m (lhs is DynamicSliced) or n (rhs is
+ * DynamicSliced), with the global result shape. Output shard r is
+ *     y_r = sum over q = r-1, r-2, ..., r (mod N) of (lhs_q @ rhs_q)[shard r],
+ * the ring order in which the accumulated shard travels {j -> j-1} so that
+ * its ID equals the partition ID at the loop end, accumulated in fp32 and
+ * stored once.
+ */
+coco_status coco_looped_einsum_rs(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                  const coco_tensor* out, void* stream);
+
+/* ------------------------------------------------------------- utilities */
+
+/*
+ * Writes mask[i] = 1 if element (first_index + i) is kept by the dropout of
+ * coco_fused_allreduce with (seed, dropout_p), else 0, for i < count.
+ * `mask` is a device pointer to `count` bytes (no alignment rule). Computed by
+ * the same device code as the fused kernel; for bit-exact comparison.
+ */
+coco_status coco_dropout_keep_mask(uint64_t seed, float dropout_p, uint64_t first_index,
+                                   uint64_t count, uint8_t* mask, void* stream);
+
+/*
+ * Synchronises `stream`, then reports and clears the device-side error word
+ * (COCO_ERR_TIMEOUT if a bounded wait in a kernel gave up since the last
+ * call). Returns COCO_ERR_CUDA if the synchronisation itself fails.
+ */
+coco_status coco_device_status(void* stream);
+
+/*
+ * Number of kernels this library has launched in this process so far (all
+ * threads, all devices). Launch accounting for benchmarks and tests.
+ */
+uint64_t coco_kernel_launches(void);
+
+/* The cudaError_t (as int) of the most recent COCO_ERR_CUDA on this thread. */
+int coco_last_cuda_error(void);
+
+/* A static, human-readable name for a status code. */
+const char* coco_status_string(coco_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int coco_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COCO_H_ */

@@ -81,13 +81,17 @@ def keep_mask(seed, p, index):
     return (counter_hash(seed, index) >> np.uint64(40)) < np.uint64(t)
 
 
-def fused_allreduce(partials, bias=None, residual=None, p=0.0, seed=0):
+def fused_allreduce(partials, bias=None, residual=None, p=0.0, seed=0, index=None):
     """The value every rank holds after [CoCoNet] Fig. 3's lines 9-13.
 
     ``partials[r]`` is rank r's local tensor; ``bias`` is a 1-D tensor over the
     last dimension (PyTorch broadcast, the only broadcast the interface
     accepts) or None; ``residual`` is the replicated residual or None. Returns
     one float64 array (the replicated result).
+
+    ``index`` (optional, same shape as the partials) gives each value's element
+    index in the full per-rank tensor, for evaluating a sample of rows; the
+    default is the row-major position inside the given arrays.
     """
     total = None
     for x in partials:  # AllReduce, summed in rank order
@@ -99,7 +103,8 @@ def fused_allreduce(partials, bias=None, residual=None, p=0.0, seed=0):
             raise ValueError("bias must be 1-D over the last dimension")
         v = v + b
     if float(np.float32(p)) != 0.0:
-        keep = keep_mask(seed, p, np.arange(v.size, dtype=np.uint64)).reshape(v.shape)
+        idx = np.arange(v.size, dtype=np.uint64) if index is None else np.asarray(index, np.uint64).ravel()
+        keep = keep_mask(seed, p, idx).reshape(v.shape)
         v = np.where(keep, v * dropout_scale(p), 0.0)
     if residual is not None:
         v = v + np.asarray(residual, np.float64)

@@ -1,0 +1,201 @@
+"""Host-side tests of the C-ABI: the library loads, exports every symbol the
+header declares, and rejects invalid arguments before any CUDA call.
+
+These run without a GPU: all device pointers are fake addresses that the
+library validates but never dereferences, and every case returns before the
+first CUDA call (an error status, or COCO_OK for an empty tensor).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def coco():
+    __graft_entry__.build()
+    from collective_fusedallreduce_gb300 import coco as c
+    return c
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "coco.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(coco_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for want in ["coco_fused_allreduce", "coco_allreduce_rs_ag", "coco_allgather", "coco_reduce_scatter",
+                 "coco_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs", "coco_einsum",
+                 "coco_status_string"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(coco):
+    lib = ctypes.CDLL(coco.library_path())
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    assert sorted(coco.EXPORTED) == header_functions()
+
+
+def test_status_strings(coco):
+    for code, name in coco.STATUS.items():
+        assert coco._lib.coco_status_string(code).decode().startswith(name)
+    assert coco.version() >= 100
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def mk(coco, dtype, layout, shape, nranks, ngroups=1, slice_dim=-1, base=FAKE, stride=1 << 32, ptrs=None):
+    t = coco.CocoTensor()
+    t.dtype, t.layout, t.ndim, t.slice_dim = dtype, layout, len(shape), slice_dim
+    for i, s in enumerate(shape):
+        t.shape[i] = s
+    t.nranks, t.ngroups = nranks, ngroups
+    for i in range(min(nranks * ngroups, coco.MAX_PTRS)):
+        t.ptr[i] = ptrs[i] if ptrs is not None else base + i * stride
+    return t
+
+
+def far(coco, partials, out, residual=None, bias=None, p=0.0):
+    return coco.raw_call("coco_fused_allreduce", ctypes.byref(partials), bias,
+                         None if residual is None else ctypes.byref(residual), p, 0, ctypes.byref(out), None)
+
+
+def test_far_validation(coco):
+    F16, L, R, S = coco.F16, coco.LOCAL, coco.REPLICATED, coco.SLICED
+    good_in = mk(coco, F16, L, (4, 16), 2)
+    good_out = mk(coco, F16, R, (4, 16), 2, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_fused_allreduce", None, None, None, 0.0, 0, ctypes.byref(good_out), None) == 1
+    # layouts
+    assert far(coco, mk(coco, F16, R, (4, 16), 2), good_out) == 4
+    assert far(coco, good_in, mk(coco, F16, L, (4, 16), 2, base=FAKE + (1 << 40))) == 4
+    # dtypes
+    assert far(coco, good_in, mk(coco, coco.BF16, R, (4, 16), 2, base=FAKE + (1 << 40))) == 3
+    bad = mk(coco, F16, L, (4, 16), 2)
+    bad.dtype = 7
+    assert far(coco, bad, good_out) == 3
+    # shapes / ranks
+    assert far(coco, good_in, mk(coco, F16, R, (4, 24), 2, base=FAKE + (1 << 40))) == 2
+    assert far(coco, good_in, mk(coco, F16, R, (4, 16), 4, base=FAKE + (1 << 40))) == 2
+    bad = mk(coco, F16, L, (4, 16), 2)
+    bad.ndim = 4
+    assert far(coco, bad, good_out) == 2
+    bad = mk(coco, F16, L, (4, 16), 33, ngroups=2)
+    assert far(coco, bad, good_out) == 2
+    # alignment: pointer and inner dimension
+    assert far(coco, mk(coco, F16, L, (4, 16), 2, base=FAKE + 8), good_out) == 5
+    assert far(coco, mk(coco, F16, L, (4, 12), 2), mk(coco, F16, R, (4, 12), 2, base=FAKE + (1 << 40))) == 5
+    assert far(coco, good_in, good_out, bias=ctypes.c_void_p(FAKE + (1 << 41) + 4)) == 5
+    # null pointers
+    assert far(coco, mk(coco, F16, L, (4, 16), 2, ptrs=[FAKE, 0]), good_out) == 1
+    # dropout probability
+    assert far(coco, good_in, good_out, p=1.5) == 10
+    assert far(coco, good_in, good_out, p=-0.1) == 10
+    assert far(coco, good_in, good_out, p=float("nan")) == 10
+    # residual
+    assert far(coco, good_in, good_out, residual=mk(coco, F16, L, (4, 16), 2, base=FAKE + (1 << 42))) == 4
+    assert far(coco, good_in, good_out, residual=mk(coco, F16, R, (8, 16), 2, base=FAKE + (1 << 42))) == 2
+
+
+def test_far_aliasing(coco):
+    F16, L, R = coco.F16, coco.LOCAL, coco.REPLICATED
+    nbytes = 4 * 16 * 2
+    ins = mk(coco, F16, L, (4, 16), 2, stride=1 << 20)
+    # output shifted into the middle of an input: partial overlap
+    out = mk(coco, F16, R, (4, 16), 2, ptrs=[FAKE + 16, FAKE + (1 << 30)])
+    assert far(coco, ins, out) == 6
+    # two distinct outputs overlapping each other
+    out = mk(coco, F16, R, (4, 16), 2, ptrs=[FAKE + (1 << 30), FAKE + (1 << 30) + 32])
+    assert far(coco, ins, out) == 6
+    # bias inside an output
+    out = mk(coco, F16, R, (4, 16), 2, ptrs=[FAKE + (1 << 30)] * 2)
+    assert far(coco, ins, out, bias=ctypes.c_void_p(FAKE + (1 << 30) + 32)) == 6
+    assert nbytes > 32
+
+
+def test_empty_tensors_return_ok_without_cuda(coco):
+    F32, L, R, S = coco.F32, coco.LOCAL, coco.REPLICATED, coco.SLICED
+    e_in = mk(coco, F32, L, (0, 16), 2)
+    e_out = mk(coco, F32, R, (0, 16), 2, base=FAKE + (1 << 40))
+    assert far(coco, e_in, e_out) == 0
+    assert coco.raw_call("coco_allreduce", ctypes.byref(e_in), ctypes.byref(e_out), None) == 0
+    e_sl = mk(coco, F32, S, (0, 16), 2, slice_dim=0, base=FAKE + (1 << 41))
+    assert coco.raw_call("coco_reduce_scatter", ctypes.byref(e_in), ctypes.byref(e_sl), None) == 0
+    assert coco.raw_call("coco_allgather", ctypes.byref(e_sl), ctypes.byref(e_out), None) == 0
+    assert coco.raw_call("coco_dropout_keep_mask", 0, ctypes.c_float(0.1), 0, 0, None, None) == 0
+    assert coco.raw_call("coco_dropout_keep_mask", 0, ctypes.c_float(0.1), 0, 5, None, None) == 1
+    # einsum with an empty output
+    lhs = mk(coco, F32, S, (0, 16), 2, slice_dim=0)
+    rhs = mk(coco, F32, L, (16, 8), 2, base=FAKE + (1 << 41))
+    out = mk(coco, F32, L, (0, 8), 2, base=FAKE + (1 << 42))
+    assert coco.raw_call("coco_looped_ag_einsum", b"mk,kn->mn", ctypes.byref(lhs), ctypes.byref(rhs),
+                         ctypes.byref(out), None) == 0
+
+
+def test_slice_validation(coco):
+    F32, L, R, S = coco.F32, coco.LOCAL, coco.REPLICATED, coco.SLICED
+    ins = mk(coco, F32, L, (24, 16), 4)
+    # uneven slice: 24 rows do not split into... 24 % 4 == 0, so use 6 ranks of 4 rows is fine; 5 is not
+    bad = mk(coco, F32, S, (24, 16), 5, slice_dim=0, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_reduce_scatter", ctypes.byref(mk(coco, F32, L, (24, 16), 5)), ctypes.byref(bad), None) == 2
+    # slice_dim out of range
+    bad = mk(coco, F32, S, (24, 16), 4, slice_dim=2, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_reduce_scatter", ctypes.byref(ins), ctypes.byref(bad), None) == 2
+    # slice of the inner dimension that is not a multiple of 8 elements
+    bad = mk(coco, F32, S, (24, 16), 4, slice_dim=1, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_reduce_scatter", ctypes.byref(ins), ctypes.byref(bad), None) == 5
+    # wrong layouts
+    good = mk(coco, F32, S, (24, 16), 4, slice_dim=0, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_reduce_scatter", ctypes.byref(good), ctypes.byref(good), None) == 4
+    assert coco.raw_call("coco_allgather", ctypes.byref(ins), ctypes.byref(mk(coco, F32, R, (24, 16), 4)), None) == 4
+    # global shape mismatch
+    bad = mk(coco, F32, S, (48, 16), 4, slice_dim=0, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_reduce_scatter", ctypes.byref(ins), ctypes.byref(bad), None) == 2
+    # reduce-scatter output overlapping an input
+    bad = mk(coco, F32, S, (24, 16), 4, slice_dim=0, base=FAKE + 64)
+    assert coco.raw_call("coco_reduce_scatter", ctypes.byref(ins), ctypes.byref(bad), None) == 6
+    # rs-ag: scratch overlapping the output
+    out = mk(coco, F32, R, (24, 16), 4, base=FAKE + (1 << 41))
+    scr = mk(coco, F32, S, (24, 16), 4, slice_dim=0, base=FAKE + (1 << 41) + 64)
+    assert coco.raw_call("coco_allreduce_rs_ag", ctypes.byref(ins), ctypes.byref(scr), ctypes.byref(out), None) == 6
+
+
+def ein(coco, name, spec, lhs, rhs, out):
+    return coco.raw_call(name, spec, ctypes.byref(lhs), ctypes.byref(rhs), ctypes.byref(out), None)
+
+
+def test_einsum_validation(coco):
+    B16, L, R, S = coco.BF16, coco.LOCAL, coco.REPLICATED, coco.SLICED
+    lhs = mk(coco, B16, S, (64, 32), 4, slice_dim=0)
+    rhs = mk(coco, B16, L, (32, 16), 4, base=FAKE + (1 << 40))
+    out = mk(coco, B16, L, (64, 16), 4, base=FAKE + (1 << 41))
+    A = "coco_looped_ag_einsum"
+    assert ein(coco, A, b"mk,kn->nm", lhs, rhs, out) == 7            # unsupported spec
+    assert ein(coco, A, b"bmk,bkn->bmn", lhs, rhs, out) == 2         # rank of operands vs spec
+    assert ein(coco, A, b"mk,kn->mn", lhs, mk(coco, coco.F16, L, (32, 16), 4, base=FAKE + (1 << 40)), out) == 3
+    assert ein(coco, A, b"mk,kn->mn", mk(coco, B16, L, (16, 32), 4), rhs, out) == 4   # nothing looped
+    assert ein(coco, A, b"mk,kn->mn", lhs, mk(coco, B16, S, (32, 16), 4, slice_dim=0, base=FAKE + (1 << 40)), out) == 4
+    assert ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, B16, R, (64, 16), 4, base=FAKE + (1 << 41))) == 4
+    assert ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, B16, L, (16, 16), 4, base=FAKE + (1 << 41))) == 2
+    assert ein(coco, A, b"mk,kn->mn", lhs, mk(coco, B16, L, (24, 16), 4, base=FAKE + (1 << 40)), out) == 2
+    # output overlapping the local operand
+    assert ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, B16, L, (64, 16), 4, base=FAKE + (1 << 40) + 16)) == 6
+    RS = "coco_looped_einsum_rs"
+    l2 = mk(coco, B16, S, (64, 32), 4, slice_dim=1)
+    r2 = mk(coco, B16, S, (32, 16), 4, slice_dim=0, base=FAKE + (1 << 40))
+    o2 = mk(coco, B16, S, (64, 16), 4, slice_dim=0, base=FAKE + (1 << 41))
+    assert ein(coco, RS, b"mk,kn->mn", lhs, r2, o2) == 4     # lhs not sliced on k
+    assert ein(coco, RS, b"mk,kn->mn", l2, r2, mk(coco, B16, L, (16, 16), 4, base=FAKE + (1 << 41))) == 4
+    assert ein(coco, RS, b"mk,kn->mn", l2, r2, mk(coco, B16, S, (64, 24), 4, slice_dim=0, base=FAKE + (1 << 41))) == 2
+    E = "coco_einsum"
+    assert ein(coco, E, b"mk,kn->mn", lhs, rhs, out) == 4    # lhs sliced on m is not a local matmul
+    assert ein(coco, E, b"mk,kn->mn", l2, r2, mk(coco, B16, R, (64, 16), 4, base=FAKE + (1 << 41))) == 4
