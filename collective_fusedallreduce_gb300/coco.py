@@ -69,6 +69,7 @@ for _name, _args in {
     "coco_reduce_scatter": [_P, _P, _S],
     "coco_allgather": [_P, _P, _S],
     "coco_allreduce_rs_ag": [_P, _P, _P, _S],
+    "coco_allreduce_rs_ag_noalloc": [_P, _P, _S],
     "coco_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
     "coco_looped_ag_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
     "coco_looped_einsum_rs": [ctypes.c_char_p, _P, _P, _P, _S],
@@ -86,6 +87,7 @@ _lib.coco_kernel_launches.restype = ctypes.c_uint64
 
 EXPORTED = [
     "coco_fused_allreduce", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
+    "coco_allreduce_rs_ag_noalloc",
     "coco_einsum", "coco_looped_ag_einsum", "coco_looped_einsum_rs", "coco_dropout_keep_mask",
     "coco_device_status", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
 ]
@@ -189,6 +191,11 @@ def coco_allgather(inp, out, stream=None):
 
 def coco_allreduce_rs_ag(inp, scratch, out, stream=None):
     _check(_lib.coco_allreduce_rs_ag(_ref(inp), _ref(scratch), _ref(out), _stream(stream)), "coco_allreduce_rs_ag")
+
+
+def coco_allreduce_rs_ag_noalloc(inp, out, stream=None):
+    """RS-AG with the library's fixed scratch array (for callers that cannot allocate)."""
+    _check(_lib.coco_allreduce_rs_ag_noalloc(_ref(inp), _ref(out), _stream(stream)), "coco_allreduce_rs_ag_noalloc")
 
 
 def coco_einsum(spec, lhs, rhs, out, stream=None):

@@ -152,6 +152,30 @@ coco_status coco_allgather(const coco_tensor* in, const coco_tensor* out, void* 
 coco_status coco_allreduce_rs_ag(const coco_tensor* in, const coco_tensor* scratch,
                                  const coco_tensor* out, void* stream);
 
+/*
+ * AllReduce Split RS-AG for callers that cannot allocate device memory. The
+ * pages have no counterpart of this entry point; it exists for code that may
+ * not call cudaMalloc once running (a latency-critical loop where an
+ * allocation could stall or fail mid-step, or a plug-in inside an application
+ * that owns all device memory). Same result as coco_allreduce_rs_ag (in LOCAL,
+ * out REPLICATED, same dtype and shape), but the sliced intermediate lives in
+ * a fixed 16 MiB array inside libcoco that every GPU loading the library
+ * holds until the process exits, split on dimension 0.
+ *   - A call needs ngroups * numel * element-size bytes (plus per-slice
+ *     rounding to 256 bytes); larger requests return COCO_ERR_UNSUPPORTED
+ *     before any CUDA call.
+ *   - The first call on a device (with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents
+ *     (nothing needs to start at zero: the ReduceScatter writes every element
+ *     the AllGather reads). Calls whose kernels can overlap on the GPU race on
+ *     it; calls ordered on one stream do not.
+ *   - It allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ *     library routine).
+ */
+coco_status coco_allreduce_rs_ag_noalloc(const coco_tensor* in, const coco_tensor* out, void* stream);
+
 /* ---------------------------------------------------------------- einsums */
 
 /*
