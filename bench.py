@@ -556,6 +556,23 @@ def load_traffic(kernel_key):
     return None
 
 
+# ------------------------------------------------------- multi-GPU helpers
+
+
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's ``x`` (the slowest replica sets the time)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(ideal_s, step_s, world):
+    """Whole-job throughput: every replica processes one step's work per ``step_s``."""
+    return 100.0 * ideal_s / step_s * world
+
+
 # ------------------------------------------------------------------- main
 
 
@@ -657,14 +674,11 @@ def main():
     elapsed = start.elapsed_time(end) / 1000.0
     per_kernel = [sum(marks[k][i].elapsed_time(marks[k][i + 1]) for k in range(args.steps)) / 1000.0 / args.steps
                   for i in range(nk)]
-    if dist is not None:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(elapsed, dist, dev)
 
     step_s = elapsed / args.steps
     ideal = wl.ideal_seconds(peaks)
-    value = 100.0 * ideal / step_s * world
+    value = aggregate_value(ideal, step_s, world)
 
     # dominant timed segment's roofline, timed with events on the launching stream
     i_dom = int(np.argmax(per_kernel))
@@ -708,12 +722,8 @@ def main():
             host_out.copy_(result, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        et = e0.elapsed_time(e1) / 1000.0
-        if dist is not None:
-            t = torch.tensor([et], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            et = float(t.item())
-        line["e2e"] = {"value": 100.0 * ideal / (et / ek) * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        et = max_over_ranks(e0.elapsed_time(e1) / 1000.0, dist, dev)
+        line["e2e"] = {"value": aggregate_value(ideal, et / ek, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "steps": ek, "ms_per_step": 1000.0 * et / ek}
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -184,6 +184,9 @@ OutView make_out(void* p, Dims3 d) {
   o.ptr = p;
   o.ld = d.c;
   o.bstride = d.r * d.c;
+  o.nb = static_cast<int32_t>(d.b);
+  o.rows = static_cast<int32_t>(d.r);
+  o.cols = static_cast<int32_t>(d.c);
   return o;
 }
 

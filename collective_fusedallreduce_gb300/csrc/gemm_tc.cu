@@ -42,9 +42,9 @@ constexpr int B_BOX_BYTES = BK * 64 * 2;         // 8 KB (64 k-rows x 128 B)
 constexpr int B_BYTES = B_BOX_BYTES * (BN / 64);  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
 constexpr int EPI_WARPS = 4;
-constexpr int EPI_STRIP = 32 * 128;                 // per warp: 32 rows x 128 B
+constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 B
 constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * EPI_STRIP;
+constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_STRIP;  // two strips per epilogue warp
 constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
 constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
@@ -52,13 +52,14 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int GROUP_M = 16;  // tile rasterisation: 16 m-tiles per group, n-major inside
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-constexpr int MAX_MAPS = 96;
+constexpr int MAX_MAPS = 80;
 constexpr int MAX_JOBS = 128;
-constexpr int MAX_SEGS = 256;
-constexpr int MAX_OUTS = 64;
+constexpr int MAX_SEGS = 192;
+constexpr int MAX_OUTS = 32;
 
 struct TcParams {
   CUtensorMap maps[MAX_MAPS];
+  CUtensorMap omaps[MAX_OUTS];  // output maps: box {128 bytes of columns, 32 rows, 1}
   Job jobs[MAX_JOBS];
   Seg segs[MAX_SEGS];
   OutView outs[MAX_OUTS];
@@ -122,6 +123,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "[%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Bulk tensor store of one 32-row strip; completion tracked per thread in bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most one committed bulk group may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -366,12 +383,13 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   } else {
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    const uint32_t strip = sbase + EPI_OFF + (warp - 2) * EPI_STRIP;
+    const uint32_t strips = sbase + EPI_OFF + (warp - 2) * 2 * EPI_STRIP;
     const int out_dt = P.out_dtype;
     const int esize = out_dt == COCO_F32 ? 4 : 2;
-    const int cols_per_chunk = 128 / esize;  // 32 (fp32) or 64 (16-bit)
+    const int cols_per_chunk = 128 / esize;  // 32 (fp32) or 64 (16-bit): one 128-byte strip row
     const int vec_elems = 16 / esize;
     int local = 0;
+    int buf = 0;
     for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++local) {
       const Tile T = decode_tile(P, t);
       const Job& J = P.jobs[T.job];
@@ -387,53 +405,69 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       const int row0 = T.mt * BM + quarter * 32;  // job-relative row of this warp's lane 0
+      // A bulk store clips only at the tensor's edges, so it is used when the
+      // tile lies inside its job's region or overhangs only past the tensor.
+      const bool bulk = (T.mt * BM + BM <= J.m || J.o_r0 + J.m == O.rows) &&
+                        (T.nt * BN + BN <= J.n || J.o_c0 + J.n == O.cols);
       const int64_t obatch = static_cast<int64_t>(J.o_b0 + T.bb) * O.bstride;
       for (int c0 = 0; c0 < BN; c0 += cols_per_chunk) {
-        // TMEM -> registers -> swizzled strip (row = lane, 8 chunks of 16 B)
-        uint32_t r[32];
+        const bool last = c0 + cols_per_chunk >= BN;
+        uint32_t p[32];
         if (out_dt == COCO_F32) {
-          tmem_ld32(tbase + c0, r);
+          tmem_ld32(tbase + c0, p);
           tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
-                         r[4 * c + 3]);
         } else {
-          uint32_t r2[32];
+          uint32_t r[32], r2[32];
           tmem_ld32(tbase + c0, r);
           tmem_ld32(tbase + c0 + 32, r2);
           tmem_ld_wait();
-          uint32_t p[32];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             p[i] = cvt_pair(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), out_dt);
             p[16 + i] = cvt_pair(__uint_as_float(r2[2 * i]), __uint_as_float(r2[2 * i + 1]), out_dt);
           }
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2],
-                         p[4 * c + 3]);
         }
+        if (last) {  // the accumulator is in registers: hand TMEM back to the MMA warp now
+          tc_fence_before();
+          mbar_arrive(tempty_bar(acc));
+        }
+        // the strip about to be overwritten was handed to a bulk store two chunks ago
+        if (lane == 0) bulk_wait_read_le1();
         __syncwarp();
-        // strip -> global: 8 lanes per 128-byte row segment, 4 rows per pass
-        const int ch = lane & 7;
-        const int col = T.nt * BN + c0 + ch * vec_elems;  // job-relative column
+        const uint32_t strip = strips + buf * EPI_STRIP;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int rr = it * 4 + (lane >> 3);
-          const int row = row0 + rr;
-          const uint4 v = ld_shared_v4(strip + rr * 128 + ((ch ^ (rr & 7)) << 4));
-          if (row < J.m && col < J.n) {
-            const int64_t off = obatch + static_cast<int64_t>(J.o_r0 + row) * O.ld + (J.o_c0 + col);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(O.ptr) + off * esize);
-            *dst = v;
+        for (int c = 0; c < 8; ++c)  // row = lane, 16-byte chunk c at its 128-byte-swizzle slot
+          st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2],
+                       p[4 * c + 3]);
+        if (bulk) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&P.omaps[J.out], strip, J.o_c0 + T.nt * BN + c0, J.o_r0 + row0, J.o_b0 + T.bb);
+            bulk_commit();
           }
+        } else {
+          __syncwarp();
+          // strip -> global: 8 lanes per 128-byte row segment, 4 rows per pass, bounded by the job
+          const int ch = lane & 7;
+          const int col = T.nt * BN + c0 + ch * vec_elems;  // job-relative column
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int rr = it * 4 + (lane >> 3);
+            const int row = row0 + rr;
+            const uint4 v = ld_shared_v4(strip + rr * 128 + ((ch ^ (rr & 7)) << 4));
+            if (row < J.m && col < J.n) {
+              const int64_t off = obatch + static_cast<int64_t>(J.o_r0 + row) * O.ld + (J.o_c0 + col);
+              *reinterpret_cast<uint4*>(static_cast<char*>(O.ptr) + off * esize) = v;
+            }
+          }
+          __syncwarp();
         }
-        __syncwarp();
+        buf ^= 1;
       }
-      tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
     }
+    if (lane == 0) bulk_wait_all();  // bulk stores finish before the CTA's shared memory goes away
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -480,6 +514,24 @@ bool encode_view(CUtensorMap* map, const View& v, int dtype, bool is_a) {
   CUresult r = enc(map, dt, 3, const_cast<void*>(v.ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Output map: [nb][rows][cols] of the output dtype, box {128 bytes of columns, 32 rows, 1}, 128B swizzle.
+bool encode_out(CUtensorMap* map, const OutView& o, int dtype) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int es = dtype == COCO_F32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(o.cols), static_cast<cuuint64_t>(o.rows),
+                        static_cast<cuuint64_t>(o.nb)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(o.ld) * es, static_cast<cuuint64_t>(o.bstride) * es};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = dtype == COCO_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype == COCO_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = enc(map, dt, 3, o.ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -548,6 +600,7 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
       if (status != cudaSuccess) break;
       if (omap[J.out] < 0) {
         P->outs[nouts] = plan.outs[J.out];
+        if (!encode_out(&P->omaps[nouts], plan.outs[J.out], plan.out_dtype)) { status = cudaErrorInvalidValue; break; }
         omap[J.out] = nouts++;
       }
       nj.out = omap[J.out];

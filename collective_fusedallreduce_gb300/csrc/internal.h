@@ -65,9 +65,11 @@ struct View {
   int64_t ld, bstride;
 };
 
+// A dense row-major [nb][rows][cols] output (elements).
 struct OutView {
   void* ptr;
   int64_t ld, bstride;
+  int32_t nb, rows, cols;
 };
 
 // One contiguous K range of a job: the A operand is read at

@@ -1,0 +1,77 @@
+"""bench.py's multi-process host logic on CPU: gloo, world size 2.
+
+Covers the max-over-ranks timing and whole-job aggregation the bench uses
+under torchrun, and the reference arm's rank handling (rank 0 alone runs and
+prints; the other ranks exit 0 without work).
+"""
+
+import json
+import os
+import subprocess
+import sys
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local = 0.010 + 0.005 * rank  # rank 1 is the slow replica
+        slowest = bench.max_over_ranks(local, dist, torch.device("cpu"))
+        q.put((rank, slowest, bench.aggregate_value(0.002, slowest, world)))
+    finally:
+        dist.destroy_process_group()
+
+
+def _free_port():
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def test_max_over_ranks_and_aggregate_with_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, slowest, value in got:
+        assert abs(slowest - 0.015) < 1e-12  # every rank sees the slowest replica's time
+        assert abs(value - 100.0 * 0.002 / 0.015 * 2) < 1e-9
+
+
+def test_single_process_helpers_without_a_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(0.5, None, None) == 0.5
+    assert abs(bench.aggregate_value(1.0, 2.0, 1) - 50.0) < 1e-12
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "2", "--warmup", "1", "--reference-seconds", "2"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    p = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1  # rank 0 alone prints
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
