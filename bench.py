@@ -235,6 +235,45 @@ class MegatronTail(Workload):
         return self.rows
 
 
+class MegatronTailFused(MegatronTail):
+    """The same Fig. 3 tail with the MatMul fused into the FusedAllReduce: one
+    tensor-core kernel sums the 8 ranks' K-slices in TMEM and applies bias,
+    dropout and residual in its epilogue; no per-rank partial is stored."""
+
+    name = "megatron_attention_tail_fused"
+
+    def __init__(self, dev, **kw):
+        super().__init__(dev, **kw)
+        self.config = dict(self.config)
+        self.config["workload"] = self.config["workload"].replace(
+            "local MatMul -> FusedAllReduce", "MatMul fused into FusedAllReduce (one kernel, no partials)")
+
+    def kernels(self):
+        n, rows, h, ks = self.n, self.rows, self.h, self.ks
+        flops = 2.0 * n * rows * ks * h
+        return [("k_gemm_tc<fused allreduce> (8 ranks' K-slices, bias+dropout+residual, 8 replicas)", "tensor",
+                 flops, 1)]
+
+    def min_bytes(self):
+        n, rows, h, ks = self.n, self.rows, self.h, self.ks
+        return (n * rows * ks + n * ks * h + rows * h + h + n * rows * h) * 2
+
+    def ideal_seconds(self, peaks):
+        # the fused computation's own roofline: max of its compute and its minimal traffic
+        flops = self.kernels()[0][2]
+        return max(flops / (peaks["bf16_tflops"] * 1e12), self.min_bytes() / (peaks["hbm_gbs"] * 1e9))
+
+    def step(self, stream, marks=None):
+        from collective_fusedallreduce_gb300 import coco
+        if marks:
+            marks[0].record(stream)
+        coco.coco_matmul_fused_allreduce("mk,kn->mn", coco.sliced(self.inp, 1), coco.sliced(self.w, 0), self.bias,
+                                         coco.replicated([self.res] * self.n), self.p, self.seed,
+                                         coco.replicated(self.out), stream)
+        if marks:
+            marks[1].record(stream)
+
+
 class LoopedCase1(Workload):
     """Looped AllGather-Einsum case 1: A[16384,8192] sliced on rows over 8 ranks, B_r[8192,3072] local, bf16."""
 
@@ -489,7 +528,7 @@ class RsAg(Workload):
         return self.numel // 4096
 
 
-WORKLOADS = {"c2": MegatronTail, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
+WORKLOADS = {"c2": MegatronTail, "c2f": MegatronTailFused, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
              "c5b": RsAg}
 
 

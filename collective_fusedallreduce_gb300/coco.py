@@ -71,6 +71,8 @@ for _name, _args in {
     "coco_allreduce_rs_ag": [_P, _P, _P, _S],
     "coco_allreduce_rs_ag_noalloc": [_P, _P, _S],
     "coco_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
+    "coco_matmul_fused_allreduce": [ctypes.c_char_p, _P, _P, ctypes.c_void_p, _P, ctypes.c_float, ctypes.c_uint64,
+                                    _P, _S],
     "coco_looped_ag_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
     "coco_looped_einsum_rs": [ctypes.c_char_p, _P, _P, _P, _S],
     "coco_dropout_keep_mask": [ctypes.c_uint64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p, _S],
@@ -88,7 +90,7 @@ _lib.coco_kernel_launches.restype = ctypes.c_uint64
 EXPORTED = [
     "coco_fused_allreduce", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
     "coco_allreduce_rs_ag_noalloc",
-    "coco_einsum", "coco_looped_ag_einsum", "coco_looped_einsum_rs", "coco_dropout_keep_mask",
+    "coco_einsum", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs", "coco_dropout_keep_mask",
     "coco_device_status", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
 ]
 
@@ -200,6 +202,13 @@ def coco_allreduce_rs_ag_noalloc(inp, out, stream=None):
 
 def coco_einsum(spec, lhs, rhs, out, stream=None):
     _check(_lib.coco_einsum(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), _stream(stream)), "coco_einsum")
+
+
+def coco_matmul_fused_allreduce(spec, lhs, rhs, bias, residual, dropout_p, seed, out, stream=None):
+    bias_ptr = None if bias is None else ctypes.c_void_p(bias.data_ptr())
+    _check(_lib.coco_matmul_fused_allreduce(spec.encode(), _ref(lhs), _ref(rhs), bias_ptr, _ref(residual),
+                                            float(dropout_p), int(seed), _ref(out), _stream(stream)),
+           "coco_matmul_fused_allreduce")
 
 
 def coco_looped_ag_einsum(spec, lhs, rhs, out, stream=None):

@@ -9,6 +9,7 @@
 // Computation via Decomposition in Large Deep Learning Models", §5.1.
 
 #include <atomic>
+#include <set>
 #include <cmath>
 #include <cstring>
 #include <string>
@@ -221,6 +222,7 @@ Job make_job(int out, Dims3 ext) {
   Job j;
   std::memset(&j, 0, sizeof(j));
   j.out = out;
+  j.nout = 1;
   j.nb = static_cast<int32_t>(ext.b);
   j.m = static_cast<int32_t>(ext.r);
   j.n = static_cast<int32_t>(ext.c);
@@ -557,6 +559,83 @@ COCO_EXPORT coco_status coco_einsum(const char* spec, const coco_tensor* lhs, co
       P.jobs.push_back(J);
     }
   return finish(P, E, a.c, stream);
+}
+
+COCO_EXPORT coco_status coco_matmul_fused_allreduce(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                                    const void* bias, const coco_tensor* residual, float dropout_p,
+                                                    uint64_t seed, const coco_tensor* out, void* stream) {
+  EinsumArgs E;
+  coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
+  if (st != COCO_OK) return st;
+  if (E.spec.batched) return COCO_ERR_UNSUPPORTED;
+  if (E.lhs.layout != COCO_SLICED || E.lhs.slice_dim != 1) return COCO_ERR_LAYOUT;
+  if (E.rhs.layout != COCO_SLICED || E.rhs.slice_dim != 0) return COCO_ERR_LAYOUT;
+  if (E.out.layout != COCO_REPLICATED) return COCO_ERR_LAYOUT;
+  if (E.lhs.dtype == COCO_F32 || E.out.dtype == COCO_F32) return COCO_ERR_UNSUPPORTED;
+  const Dims3 a = dims_of(E.spec, E.lhs.local), b = dims_of(E.spec, E.rhs.local), o = dims_of(E.spec, E.out.local);
+  if (a.c != b.r || o.r != a.r || o.c != b.c) return COCO_ERR_SHAPE;
+  TInfo res;
+  if (residual) {
+    if ((st = check_tensor(residual, &res)) != COCO_OK) return st;
+    if (res.layout != COCO_REPLICATED) return COCO_ERR_LAYOUT;
+    if (res.dtype != E.out.dtype) return COCO_ERR_DTYPE;
+    if (!same_ranks(res, E.out) || !same_local_shape(res, E.out)) return COCO_ERR_SHAPE;
+  }
+  if (!(dropout_p >= 0.0f && dropout_p <= 1.0f)) return COCO_ERR_VALUE;
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & 15)) return COCO_ERR_ALIGN;
+  if (E.out.numel == 0) return COCO_OK;
+  if (a.c == 0) return COCO_ERR_UNSUPPORTED;  // no contraction: use coco_fused_allreduce on zero partials
+  // outputs: disjoint from the operands and bias; the residual may be an output exactly (each
+  // element's residual is read by the thread that computes it, before the tile is stored)
+  std::vector<Range> outs, ins, resr;
+  tensor_ranges(E.out, &outs);
+  tensor_ranges(E.lhs, &ins);
+  tensor_ranges(E.rhs, &ins);
+  if ((st = check_alias(outs, ins, false)) != COCO_OK) return st;
+  if (residual) {
+    tensor_ranges(res, &resr, true);
+    if ((st = check_alias(outs, resr, true)) != COCO_OK) return st;
+  }
+  if (bias) {
+    const Range br = range_of(bias, o.c * dtype_size(E.out.dtype));
+    for (const Range& r : outs)
+      if (overlap(r, br)) return COCO_ERR_ALIAS;
+  }
+  {  // a replica buffer belongs to one group only
+    std::set<void*> seen;
+    for (int g = 0; g < E.out.ngroups; ++g) {
+      std::set<void*> mine;
+      for (int r = 0; r < E.out.nranks; ++r) mine.insert(E.out.ptr(g, r));
+      for (void* p : mine)
+        if (!seen.insert(p).second) return COCO_ERR_ALIAS;
+    }
+  }
+
+  GemmPlan P;
+  P.mode = EPI_FUSED_ALLREDUCE;
+  P.in_dtype = E.lhs.dtype;
+  P.out_dtype = E.out.dtype;
+  P.far.bias = bias;
+  P.far.dropout = dropout_p > 0.0f;
+  const double keep = 1.0 - static_cast<double>(dropout_p);
+  P.far.keep_threshold = static_cast<uint32_t>(std::floor(keep * 16777216.0));
+  P.far.scale = dropout_p < 1.0f ? static_cast<float>(1.0 / keep) : 0.0f;
+  P.far.seed = seed;
+  const int n = E.lhs.nranks;
+  for (int g = 0; g < E.out.ngroups; ++g) {
+    Job J = make_job(static_cast<int>(P.outs.size()), o);
+    std::vector<int> reps = output_ranks(E.out, g);
+    for (int r : reps) P.outs.push_back(make_out(E.out.ptr(g, r), o));
+    J.nout = static_cast<int16_t>(reps.size());
+    J.res = residual ? res.ptr(g, 0) : nullptr;
+    J.seg0 = static_cast<int16_t>(P.segs.size());
+    J.nseg = static_cast<int16_t>(n);
+    for (int r = 0; r < n; ++r)  // the AllReduce's summation order: rank 0, 1, ..., N-1
+      P.segs.push_back(make_seg(add_view(&P, make_view(E.lhs.ptr(g, r), a)),
+                                add_view(&P, make_view(E.rhs.ptr(g, r), b)), a.c));
+    P.jobs.push_back(J);
+  }
+  return run_plan(P, static_cast<cudaStream_t>(stream));
 }
 
 COCO_EXPORT coco_status coco_looped_ag_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,

@@ -36,18 +36,28 @@
 namespace coco {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BOX_BYTES = BK * 64 * 2;         // 8 KB (64 k-rows x 128 B)
 constexpr int B_BYTES = B_BOX_BYTES * (BN / 64);  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
-constexpr int EPI_WARPS = 4;
 constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 B
-constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_STRIP;  // two strips per epilogue warp
-constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
-constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+
+// Shared-memory budget per epilogue mode. The plain store keeps a 4-stage
+// operand ring and 4 epilogue warps; the FusedAllReduce epilogue does more
+// arithmetic per element, so it trades one stage for 8 epilogue warps (two
+// per TMEM lane quarter, each taking half of the tile's columns).
+template <int MODE>
+struct Cfg {
+  static constexpr int STAGES = MODE == 0 ? 4 : 3;
+  static constexpr int EPI_WARPS = MODE == 0 ? 4 : 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_STRIP;  // two strips per epilogue warp
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
+  static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int GROUP_M = 16;  // tile rasterisation: 16 m-tiles per group, n-major inside
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -69,6 +79,12 @@ struct TcParams {
   uint32_t idesc;
   int32_t out_dtype;
   unsigned int* err;
+  // FusedAllReduce epilogue (EPI_FUSED_ALLREDUCE only)
+  const void* bias;
+  uint64_t seed;
+  uint32_t keep_threshold;
+  float scale;
+  int32_t dropout;
 };
 static_assert(sizeof(TcParams) <= 32000, "kernel parameter block too large");
 
@@ -126,11 +142,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 }
 
 // Bulk tensor store of one 32-row strip; completion tracked per thread in bulk groups.
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2,
+                                             uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // At most one committed bulk group may still be reading shared memory.
@@ -255,9 +273,58 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_nc_v4_hint(const void* p, uint64_t policy) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(policy));
+  return r;
+}
+
+// Eight 16-bit values (f16 or bf16) of a 16-byte vector as floats.
+__device__ __forceinline__ void unpack8(uint4 v, int dtype, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t;
+    if (dtype == COCO_F16) t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    else t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// Dropout keep test of the FusedAllReduce: element e is kept iff the top 24
+// bits of SplitMix64 output number e+1 from state `seed` (Steele, Lea and
+// Flood, OOPSLA 2014) are below the threshold; `z` is that output's state,
+// seed + (e+1) * gamma. The finaliser's last xor-shift by 31 leaves bits
+// 40..63 unchanged, so it is not computed.
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+__device__ __forceinline__ bool keep_state(uint64_t z, uint32_t threshold) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return static_cast<uint32_t>(z >> 40) < threshold;
+}
+
 // ------------------------------------------------------------------ kernel
 
-__global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ TcParams P) {
+// MODE = EPI_STORE: store the accumulator. MODE = EPI_FUSED_ALLREDUCE: the
+// accumulator is a sum over ranks (the K-segments are the ranks' K-slices);
+// add the bias, apply dropout and add the residual in registers, then store
+// the tile to every replica of the group ([CoCoNet] §5.2, FusedAllReduce,
+// with the MatMul of its Fig. 3 fused in front).
+template <int MODE>
+__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_constant__ TcParams P) {
+  constexpr int STAGES = Cfg<MODE>::STAGES, EPI_WARPS = Cfg<MODE>::EPI_WARPS;
+  constexpr int EPI_OFF = Cfg<MODE>::EPI_OFF, BAR_OFF = Cfg<MODE>::BAR_OFF, NUM_BARS = Cfg<MODE>::NUM_BARS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -307,9 +374,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       bool ok = true;
       for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
         const Tile T = decode_tile(P, t);
-        const Job& J = P.jobs[T.job];
+        const Job J = P.jobs[T.job];  // a register copy: asm memory clobbers would force reloads
         for (int si = 0; ok && si < J.nseg; ++si) {
-          const Seg& S = P.segs[J.seg0 + si];
+          const Seg S = P.segs[J.seg0 + si];
           const CUtensorMap* ma = &P.maps[S.a];
           const CUtensorMap* mb = &P.maps[S.b];
           const int kblocks = (S.klen + BK - 1) / BK;
@@ -347,7 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       bool any_mma = false;
       for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x, ++local) {
         const Tile T = decode_tile(P, t);
-        const Job& J = P.jobs[T.job];
+        const Job J = P.jobs[T.job];  // a register copy: asm memory clobbers would force reloads
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
         if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) { fail(); ok = false; break; }
@@ -355,7 +422,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         const uint32_t d = tmem_base + acc * BN;
         uint32_t accumulate = 0;
         for (int si = 0; ok && si < J.nseg; ++si) {
-          const int kblocks = (P.segs[J.seg0 + si].klen + BK - 1) / BK;
+          const int kblocks = (static_cast<int>(P.segs[J.seg0 + si].klen) + BK - 1) / BK;
           for (int kb = 0; kb < kblocks; ++kb) {
             if (!mbar_wait(full_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
             tc_fence_after();
@@ -384,6 +451,16 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
     const uint32_t strips = sbase + EPI_OFF + (warp - 2) * 2 * EPI_STRIP;
+    // with 8 epilogue warps, warps 2..5 take columns [0, BN/2) and warps 6..9 [BN/2, BN)
+    constexpr int COLS = EPI_WARPS == 8 ? BN / 2 : BN;
+    const int col_begin = EPI_WARPS == 8 ? ((warp - 2) >> 2) * COLS : 0;
+    const uint64_t seed = P.seed;
+    const uint32_t keep_threshold = P.keep_threshold;
+    const float scale = P.scale;
+    const bool dropout = P.dropout != 0;
+    const char* bias_ptr = static_cast<const char*>(P.bias);
+    uint64_t evict_first = 0;  // L2 policy for data touched once (outputs, residual)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
     const int out_dt = P.out_dtype;
     const int esize = out_dt == COCO_F32 ? 4 : 2;
     const int cols_per_chunk = 128 / esize;  // 32 (fp32) or 64 (16-bit): one 128-byte strip row
@@ -392,8 +469,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
     int buf = 0;
     for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++local) {
       const Tile T = decode_tile(P, t);
-      const Job& J = P.jobs[T.job];
-      const OutView& O = P.outs[J.out];
+      const Job J = P.jobs[T.job];  // a register copy: asm memory clobbers would force reloads
+      const OutView O = P.outs[J.out];
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       // all lanes must agree before the warp-collective TMEM loads
@@ -410,10 +487,59 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       const bool bulk = (T.mt * BM + BM <= J.m || J.o_r0 + J.m == O.rows) &&
                         (T.nt * BN + BN <= J.n || J.o_c0 + J.n == O.cols);
       const int64_t obatch = static_cast<int64_t>(J.o_b0 + T.bb) * O.bstride;
-      for (int c0 = 0; c0 < BN; c0 += cols_per_chunk) {
-        const bool last = c0 + cols_per_chunk >= BN;
+      // FusedAllReduce: this lane's residual row segment for the next chunk is
+      // requested one chunk ahead, so its latency overlaps the current chunk.
+      const int jrow = row0 + lane;
+      const int64_t grow = J.o_r0 + jrow;
+      uint4 rv[8];
+      auto load_residual = [&](int cc) {
+        const int gc = J.o_c0 + T.nt * BN + cc;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          rv[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (J.res && jrow < J.m && gc + i * 8 < O.cols && cc < col_begin + COLS)
+            rv[i] = ld_nc_v4_hint(static_cast<const char*>(J.res) + (obatch + grow * O.ld + gc + i * 8) * 2,
+                                  evict_first);
+        }
+      };
+      if constexpr (MODE == EPI_FUSED_ALLREDUCE) load_residual(col_begin);
+      for (int c0 = col_begin; c0 < col_begin + COLS; c0 += cols_per_chunk) {
+        const bool last = c0 + cols_per_chunk >= col_begin + COLS;
         uint32_t p[32];
-        if (out_dt == COCO_F32) {
+        if constexpr (MODE == EPI_FUSED_ALLREDUCE) {
+          // 16-bit output: 64 columns of this lane's row
+          const int gcol0 = J.o_c0 + T.nt * BN + c0;
+          uint4 cur[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cur[i] = rv[i];
+          if (!last) load_residual(c0 + cols_per_chunk);
+          uint32_t r[32], r2[32];
+          tmem_ld32(tbase + c0, r);
+          tmem_ld32(tbase + c0 + 32, r2);
+          tmem_ld_wait();
+          uint64_t z = seed + (static_cast<uint64_t>(grow * O.cols + gcol0) + 1ull) * kGamma;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float bias[8], res[8], v[8];
+            if (bias_ptr && gcol0 + i * 8 < O.cols) {  // the same address in every lane: one broadcast load
+              unpack8(ld_nc_v4(bias_ptr + (gcol0 + i * 8) * 2), out_dt, bias);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) bias[j] = 0.0f;
+            }
+            unpack8(cur[i], out_dt, res);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int c = i * 8 + j;
+              float x = __uint_as_float(c < 32 ? r[c] : r2[c - 32]) + bias[j];
+              if (dropout) x = keep_state(z, keep_threshold) ? x * scale : 0.0f;
+              v[j] = x + res[j];
+              z += kGamma;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) p[i * 4 + j] = cvt_pair(v[2 * j], v[2 * j + 1], out_dt);
+          }
+        } else if (out_dt == COCO_F32) {
           tmem_ld32(tbase + c0, p);
           tmem_ld_wait();
         } else {
@@ -442,8 +568,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         if (bulk) {
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&P.omaps[J.out], strip, J.o_c0 + T.nt * BN + c0, J.o_r0 + row0, J.o_b0 + T.bb);
+          if (lane == 0) {  // one strip, stored to every replica of the job's output
+            const int nrep = MODE == EPI_STORE ? 1 : J.nout;
+            for (int o = 0; o < nrep; ++o)
+              tma_store_3d(&P.omaps[J.out + o], strip, J.o_c0 + T.nt * BN + c0, J.o_r0 + row0, J.o_b0 + T.bb,
+                           evict_first);
             bulk_commit();
           }
         } else {
@@ -458,7 +587,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
             const uint4 v = ld_shared_v4(strip + rr * 128 + ((ch ^ (rr & 7)) << 4));
             if (row < J.m && col < J.n) {
               const int64_t off = obatch + static_cast<int64_t>(J.o_r0 + row) * O.ld + (J.o_c0 + col);
-              *reinterpret_cast<uint4*>(static_cast<char*>(O.ptr) + off * esize) = v;
+              if (MODE == EPI_STORE) {
+                *reinterpret_cast<uint4*>(static_cast<char*>(O.ptr) + off * esize) = v;
+              } else {
+                for (int o = 0; o < J.nout; ++o)
+                  *reinterpret_cast<uint4*>(static_cast<char*>(P.outs[J.out + o].ptr) + off * esize) = v;
+              }
             }
           }
           __syncwarp();
@@ -535,7 +669,7 @@ bool encode_out(CUtensorMap* map, const OutView& o, int dtype) {
   return r == CUDA_SUCCESS;
 }
 
-bool smem_configured[64] = {false};
+bool smem_configured[2][64] = {{false}};
 
 }  // namespace
 
@@ -551,12 +685,16 @@ unsigned int* gemm_error_word() {
 // segment and output indices, then launches each.
 cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* err_word) {
   if (!encode_fn()) return cudaErrorNotSupported;
+  const bool far = plan.mode == EPI_FUSED_ALLREDUCE;
+  if (far && plan.out_dtype == COCO_F32) return cudaErrorNotSupported;
+  auto kernel = far ? k_gemm_tc<EPI_FUSED_ALLREDUCE> : k_gemm_tc<EPI_STORE>;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !smem_configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (dev >= 0 && dev < 64 && !smem_configured[far][dev]) {
+    const int smem = far ? Cfg<EPI_FUSED_ALLREDUCE>::SMEM_BYTES : Cfg<EPI_STORE>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    smem_configured[dev] = true;
+    smem_configured[far][dev] = true;
   }
   // A-views are used with the A box and B-views with the B box; a view used
   // on both sides gets two maps.
@@ -568,7 +706,9 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
                          (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
   while (j < plan.jobs.size() && status == cudaSuccess) {
     memset(P, 0, sizeof(TcParams));
-    std::vector<int> amap(plan.views.size(), -1), bmap(plan.views.size(), -1), omap(plan.outs.size(), -1);
+    std::vector<int> amap(plan.views.size(), -1), bmap(plan.views.size(), -1);
+    std::vector<std::pair<int, int>> orange;  // (first output, count) ranges already in this launch
+    std::vector<int> obase;
     int nmaps = 0, nsegs = 0, nouts = 0, njobs = 0, tiles = 0;
     while (j < plan.jobs.size() && njobs < MAX_JOBS) {
       const Job& J = plan.jobs[j];
@@ -579,7 +719,10 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
         need_maps += amap[S.a] < 0;
         need_maps += bmap[S.b] < 0;
       }
-      const int need_out = omap[J.out] < 0;
+      int found = -1;
+      for (size_t q = 0; q < orange.size(); ++q)
+        if (orange[q].first == J.out && orange[q].second == J.nout) found = obase[q];
+      const int need_out = found < 0 ? J.nout : 0;
       if (nmaps + need_maps > MAX_MAPS || nsegs + J.nseg > MAX_SEGS || nouts + need_out > MAX_OUTS) break;
       Job nj = J;
       nj.seg0 = static_cast<int16_t>(nsegs);
@@ -598,12 +741,18 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
         P->segs[nsegs++] = S;
       }
       if (status != cudaSuccess) break;
-      if (omap[J.out] < 0) {
-        P->outs[nouts] = plan.outs[J.out];
-        if (!encode_out(&P->omaps[nouts], plan.outs[J.out], plan.out_dtype)) { status = cudaErrorInvalidValue; break; }
-        omap[J.out] = nouts++;
+      if (found < 0) {  // the job's replicas get consecutive output slots
+        found = nouts;
+        for (int o = 0; o < J.nout && status == cudaSuccess; ++o) {
+          P->outs[nouts] = plan.outs[J.out + o];
+          if (!encode_out(&P->omaps[nouts], plan.outs[J.out + o], plan.out_dtype)) status = cudaErrorInvalidValue;
+          ++nouts;
+        }
+        if (status != cudaSuccess) break;
+        orange.emplace_back(J.out, J.nout);
+        obase.push_back(found);
       }
-      nj.out = omap[J.out];
+      nj.out = found;
       P->jobs[njobs] = nj;
       P->tile_start[njobs] = tiles;
       tiles += J.nb * ((J.m + BM - 1) / BM) * ((J.n + BN - 1) / BN);
@@ -618,8 +767,16 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
     P->idesc = idesc;
     P->out_dtype = plan.out_dtype;
     P->err = err_word;
+    P->bias = plan.far.bias;
+    P->seed = plan.far.seed;
+    P->keep_threshold = plan.far.keep_threshold;
+    P->scale = plan.far.scale;
+    P->dropout = plan.far.dropout ? 1 : 0;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    k_gemm_tc<<<grid, THREADS, SMEM_BYTES, s>>>(*P);
+    if (far)
+      kernel<<<grid, Cfg<EPI_FUSED_ALLREDUCE>::THREADS, Cfg<EPI_FUSED_ALLREDUCE>::SMEM_BYTES, s>>>(*P);
+    else
+      kernel<<<grid, Cfg<EPI_STORE>::THREADS, Cfg<EPI_STORE>::SMEM_BYTES, s>>>(*P);
     count_launch();
     status = cudaGetLastError();
   }

@@ -85,16 +85,37 @@ struct Seg {
 // A block of output: batches [o_b0, o_b0+nb), rows [o_r0, o_r0+m), cols
 // [o_c0, o_c0+n) of output `out`, the sum over segments seg0..seg0+nseg-1 in
 // that order.
+//
+// With the FusedAllReduce epilogue the job's result is written to `nout`
+// outputs (indices out .. out+nout-1, the distinct replicas of a group) and
+// `res` is the replicated residual of the same shape (or null).
 struct Job {
   int32_t out;
   int32_t o_b0, o_r0, o_c0;
   int32_t nb, m, n;
   int16_t seg0, nseg;
+  int16_t nout, pad_;
+  const void* res;
+};
+
+// The epilogue applied to every accumulator tile.
+enum EpilogueMode { EPI_STORE = 0, EPI_FUSED_ALLREDUCE = 1 };
+
+// Pointwise part of the FusedAllReduce epilogue (bias over the last
+// dimension, counter-hash dropout, then the residual), as in coco_fused_allreduce.
+struct FarEpilogue {
+  const void* bias = nullptr;  // [cols] of the output dtype, or null
+  bool dropout = false;
+  uint32_t keep_threshold = 1u << 24;
+  float scale = 1.0f;
+  uint64_t seed = 0;
 };
 
 struct GemmPlan {
   int in_dtype = COCO_BF16;
   int out_dtype = COCO_BF16;
+  int mode = EPI_STORE;
+  FarEpilogue far;
   std::vector<View> views;
   std::vector<OutView> outs;
   std::vector<Seg> segs;

@@ -197,6 +197,28 @@ coco_status coco_einsum(const char* spec, const coco_tensor* lhs, const coco_ten
                         const coco_tensor* out, void* stream);
 
 /*
+ * MatMul fused with FusedAllReduce ([CoCoNet] Fig. 3 lines 7-13; the
+ * overlap of its MatMul with the AllReduce, §5.3 / Fig. 9, taken to a single
+ * kernel on one GPU):
+ *
+ *   out_q = dropout( sum_{r=0}^{N-1} lhs_r @ rhs_r + bias ) + residual
+ *
+ * for every rank q of every group. lhs SLICED on k (per rank [m, k/N]); rhs
+ * SLICED on k (per rank [k/N, n]); lhs and rhs F16 or BF16 (the same);
+ * out REPLICATED [m, n], F16 or BF16; bias, residual, dropout_p and seed as in
+ * coco_fused_allreduce (same dtype as out; element index e = row * n + col).
+ * The sum over ranks accumulates in fp32 on the tensor cores (rank order
+ * 0..N-1) and is never written to memory: no per-rank partial exists. out_q
+ * may equal the residual pointer exactly; outputs may not overlap lhs, rhs or
+ * bias, and a buffer may be a replica of one group only (else COCO_ERR_ALIAS).
+ * A zero contraction length returns COCO_ERR_UNSUPPORTED; F32 operands or
+ * output return COCO_ERR_UNSUPPORTED.
+ */
+coco_status coco_matmul_fused_allreduce(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                        const void* bias, const coco_tensor* residual, float dropout_p,
+                                        uint64_t seed, const coco_tensor* out, void* stream);
+
+/*
  * Looped AllGather-Einsum ([Decomp] §4 Fig. 4 and §5.1, Alg. 1): exactly one
  * operand is SLICED (the looped operand); the other is LOCAL or REPLICATED
  * (the local operand). Rank r computes, for i = 0..N-1 in this order, the
