@@ -43,14 +43,14 @@ constexpr int B_BYTES = B_BOX_BYTES * (BN / 64);  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
 constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 B
 
-// Shared-memory budget per epilogue mode. The plain store keeps a 4-stage
-// operand ring and 4 epilogue warps; the FusedAllReduce epilogue does more
-// arithmetic per element, so it trades one stage for 8 epilogue warps (two
-// per TMEM lane quarter, each taking half of the tile's columns).
+// Shared-memory budget per epilogue mode: a 4-stage operand ring and four
+// epilogue warps (one per TMEM lane quarter). Eight epilogue warps (two per
+// quarter, each taking half of the columns) fit only with three stages; the
+// MMA warp does not wait on the epilogue in either mode, so four stages win.
 template <int MODE>
 struct Cfg {
-  static constexpr int STAGES = MODE == 0 ? 4 : 3;
-  static constexpr int EPI_WARPS = MODE == 0 ? 4 : 8;
+  static constexpr int STAGES = 4;
+  static constexpr int EPI_WARPS = 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_STRIP;  // two strips per epilogue warp
@@ -73,9 +73,9 @@ struct TcParams {
   Job jobs[MAX_JOBS];
   Seg segs[MAX_SEGS];
   OutView outs[MAX_OUTS];
-  int32_t tile_start[MAX_JOBS + 1];
+  int32_t unit_start[MAX_JOBS + 1];  // first work unit (a pair of vertically adjacent tiles) of each job
   int32_t njobs;
-  int32_t total_tiles;
+  int32_t total_units;
   uint32_t idesc;
   int32_t out_dtype;
   unsigned int* err;
@@ -159,6 +159,25 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The same copy, written to the same shared-memory offset of every CTA in
+// `cta_mask` and completing the mbarrier at that offset in each of them.
+__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                      int c1, int c2, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%4, "
+      "%5, %6}], [%2], %3;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "h"(cta_mask), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -185,6 +204,13 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+// The same, arriving on the mbarrier at offset `bar` of every CTA in `cta_mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -229,26 +255,30 @@ struct Tile {
   int job, bb, mt, nt;
 };
 
-__device__ __forceinline__ Tile decode_tile(const TcParams& P, int t) {
+// Work unit u is a pair of vertically adjacent 128 x 256 tiles with the same
+// column block; CTA `rank` of the cluster takes m-tile 2 * pair + rank. Units
+// are rasterised in groups of GROUP_M / 2 pairs, column-major inside a group.
+__device__ __forceinline__ Tile decode_unit(const TcParams& P, int u, int rank) {
   int lo = 0, hi = P.njobs - 1;
-  while (lo < hi) {  // last job with tile_start <= t
+  while (lo < hi) {  // last job with unit_start <= u
     const int mid = (lo + hi + 1) >> 1;
-    if (P.tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    if (P.unit_start[mid] <= u) lo = mid; else hi = mid - 1;
   }
-  const Job& J = P.jobs[lo];
-  const int mtiles = (J.m + BM - 1) / BM, ntiles = (J.n + BN - 1) / BN;
-  const int local = t - P.tile_start[lo];
-  const int per_b = mtiles * ntiles;
+  const int jm = P.jobs[lo].m, jn = P.jobs[lo].n;
+  const int mpairs = (jm + 2 * BM - 1) / (2 * BM), ntiles = (jn + BN - 1) / BN;
+  const int local = u - P.unit_start[lo];
+  const int per_b = mpairs * ntiles;
+  constexpr int GP = GROUP_M / 2;
   Tile T;
   T.job = lo;
   T.bb = local / per_b;
   const int r = local - T.bb * per_b;
-  const int group = r / (GROUP_M * ntiles);
-  const int first_m = group * GROUP_M;
-  const int gm = min(GROUP_M, mtiles - first_m);
-  const int in_g = r - group * GROUP_M * ntiles;
-  T.mt = first_m + in_g % gm;
-  T.nt = in_g / gm;
+  const int group = r / (GP * ntiles);
+  const int first = group * GP;
+  const int gp = min(GP, mpairs - first);
+  const int in_g = r - group * GP * ntiles;
+  T.mt = 2 * (first + in_g % gp) + rank;
+  T.nt = in_g / gp;
   return T;
 }
 
@@ -322,7 +352,8 @@ __device__ __forceinline__ bool keep_state(uint64_t z, uint32_t threshold) {
 // the tile to every replica of the group ([CoCoNet] §5.2, FusedAllReduce,
 // with the MatMul of its Fig. 3 fused in front).
 template <int MODE>
-__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_constant__ TcParams P) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 1)
+    k_gemm_tc(const __grid_constant__ TcParams P) {
   constexpr int STAGES = Cfg<MODE>::STAGES, EPI_WARPS = Cfg<MODE>::EPI_WARPS;
   constexpr int EPI_OFF = Cfg<MODE>::EPI_OFF, BAR_OFF = Cfg<MODE>::BAR_OFF, NUM_BARS = Cfg<MODE>::NUM_BARS;
   extern __shared__ uint8_t smem_raw[];
@@ -338,11 +369,17 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 8 * NUM_BARS + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pair: both CTAs walk the same work units; CTA `rank` takes the unit's m-tile
+  // 2 * pair + rank, loads its own A tile and half of the shared B tile, and multicasts
+  // that half into both CTAs' shared memory.
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  constexpr uint16_t kPair = 0x3;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), 2);  // freed when both CTAs' MMAs have read the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -354,7 +391,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anything is multicast into them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -372,8 +409,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) { issued[s] = false; issued_parity[s] = 0; }
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
-        const Tile T = decode_tile(P, t);
+      for (int u = cluster_id; ok && u < P.total_units; u += nclusters) {
+        const Tile T = decode_unit(P, u, rank);
         const Job J = P.jobs[T.job];  // a register copy: asm memory clobbers would force reloads
         for (int si = 0; ok && si < J.nseg; ++si) {
           const Seg S = P.segs[J.seg0 + si];
@@ -386,11 +423,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
-            mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+            mbar_expect_tx(full_bar(stage), STAGE_BYTES);  // own A + both halves of B
             tma_load_3d(sa, ma, full_bar(stage), S.a_k0 + kb * BK, arow, ab);
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb);
+            for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); ++j)  // this CTA's half of B
+              tma_load_3d_multicast(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb,
+                                    kPair);
             issued[stage] = true;
             issued_parity[stage] = phase;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -412,8 +450,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
       int local = 0;
       bool ok = true;
       bool any_mma = false;
-      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x, ++local) {
-        const Tile T = decode_tile(P, t);
+      for (int u = cluster_id; ok && u < P.total_units; u += nclusters, ++local) {
+        const Tile T = decode_unit(P, u, rank);
         const Job J = P.jobs[T.job];  // a register copy: asm memory clobbers would force reloads
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
@@ -434,7 +472,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
               accumulate = 1;
             }
             any_mma = true;
-            umma_commit(empty_bar(stage));
+            umma_commit_multicast(empty_bar(stage), kPair);  // both producers may refill this stage
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
@@ -467,8 +505,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
     const int vec_elems = 16 / esize;
     int local = 0;
     int buf = 0;
-    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x, ++local) {
-      const Tile T = decode_tile(P, t);
+    for (int u = cluster_id; u < P.total_units; u += nclusters, ++local) {
+      const Tile T = decode_unit(P, u, rank);
       const Job J = P.jobs[T.job];  // a register copy: asm memory clobbers would force reloads
       const OutView O = P.outs[J.out];
       const int acc = local & 1;
@@ -606,6 +644,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) k_gemm_tc(const __grid_
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still multicast or commit into it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -754,16 +793,16 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
       }
       nj.out = found;
       P->jobs[njobs] = nj;
-      P->tile_start[njobs] = tiles;
-      tiles += J.nb * ((J.m + BM - 1) / BM) * ((J.n + BN - 1) / BN);
+      P->unit_start[njobs] = tiles;
+      tiles += J.nb * ((J.m + 2 * BM - 1) / (2 * BM)) * ((J.n + BN - 1) / BN);
       ++njobs;
       ++j;
     }
     if (status != cudaSuccess) break;
     if (njobs == 0) { status = cudaErrorInvalidValue; break; }  // a single job exceeds the limits
-    P->tile_start[njobs] = tiles;
+    P->unit_start[njobs] = tiles;
     P->njobs = njobs;
-    P->total_tiles = tiles;
+    P->total_units = tiles;
     P->idesc = idesc;
     P->out_dtype = plan.out_dtype;
     P->err = err_word;
@@ -772,7 +811,8 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
     P->keep_threshold = plan.far.keep_threshold;
     P->scale = plan.far.scale;
     P->dropout = plan.far.dropout ? 1 : 0;
-    const int grid = tiles < sm_count() ? tiles : sm_count();
+    const int pairs = sm_count() / 2;  // persistent: one CTA pair per two SMs
+    const int grid = 2 * (tiles < pairs ? tiles : pairs);
     if (far)
       kernel<<<grid, Cfg<EPI_FUSED_ALLREDUCE>::THREADS, Cfg<EPI_FUSED_ALLREDUCE>::SMEM_BYTES, s>>>(*P);
     else
