@@ -28,6 +28,7 @@ MAX_DIMS = 3
 
 F32, F16, BF16 = 0, 1, 2
 LOCAL, SLICED, REPLICATED = 0, 1, 2
+SCHED_RING, SCHED_UNROLL2, SCHED_BIDIRECTIONAL = 0, 1, 2
 
 STATUS = {
     0: "COCO_OK", 1: "COCO_ERR_NULL", 2: "COCO_ERR_SHAPE", 3: "COCO_ERR_DTYPE", 4: "COCO_ERR_LAYOUT",
@@ -75,6 +76,8 @@ for _name, _args in {
                                     _P, _S],
     "coco_looped_ag_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
     "coco_looped_einsum_rs": [ctypes.c_char_p, _P, _P, _P, _S],
+    "coco_looped_ag_einsum_sched": [ctypes.c_char_p, _P, _P, _P, ctypes.c_int, _S],
+    "coco_looped_einsum_rs_sched": [ctypes.c_char_p, _P, _P, _P, ctypes.c_int, _S],
     "coco_dropout_keep_mask": [ctypes.c_uint64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p, _S],
     "coco_device_status": [_S],
 }.items():
@@ -90,7 +93,8 @@ _lib.coco_kernel_launches.restype = ctypes.c_uint64
 EXPORTED = [
     "coco_fused_allreduce", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
     "coco_allreduce_rs_ag_noalloc",
-    "coco_einsum", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs", "coco_dropout_keep_mask",
+    "coco_einsum", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs",
+    "coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched", "coco_dropout_keep_mask",
     "coco_device_status", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
 ]
 
@@ -219,6 +223,16 @@ def coco_looped_ag_einsum(spec, lhs, rhs, out, stream=None):
 def coco_looped_einsum_rs(spec, lhs, rhs, out, stream=None):
     _check(_lib.coco_looped_einsum_rs(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), _stream(stream)),
            "coco_looped_einsum_rs")
+
+
+def coco_looped_ag_einsum_sched(spec, lhs, rhs, out, schedule, stream=None):
+    _check(_lib.coco_looped_ag_einsum_sched(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), int(schedule),
+                                            _stream(stream)), "coco_looped_ag_einsum_sched")
+
+
+def coco_looped_einsum_rs_sched(spec, lhs, rhs, out, schedule, stream=None):
+    _check(_lib.coco_looped_einsum_rs_sched(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), int(schedule),
+                                            _stream(stream)), "coco_looped_einsum_rs_sched")
 
 
 def coco_dropout_keep_mask(seed, dropout_p, first_index, count, mask, stream=None):

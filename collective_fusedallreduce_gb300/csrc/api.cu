@@ -638,8 +638,52 @@ COCO_EXPORT coco_status coco_matmul_fused_allreduce(const char* spec, const coco
   return run_plan(P, static_cast<cudaStream_t>(stream));
 }
 
-COCO_EXPORT coco_status coco_looped_ag_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
-                                              const coco_tensor* out, void* stream) {
+namespace {
+
+// The order in which rank r of n visits the shards of the looped operand.
+//   ring / unroll-by-2: r, r+1, ..., r-1 (the shard held after i permutes {j -> j-1});
+//   bidirectional: r, then r+1, r-1, r+2, r-2, ... (one shard from each direction per step).
+std::vector<int> ag_order(int r, int n, int sched) {
+  std::vector<int> o;
+  if (sched != COCO_SCHED_BIDIRECTIONAL) {
+    for (int i = 0; i < n; ++i) o.push_back((r + i) % n);
+    return o;
+  }
+  o.push_back(r);
+  for (int k = 1; static_cast<int>(o.size()) < n; ++k) {
+    o.push_back((r + k) % n);
+    if (static_cast<int>(o.size()) < n) o.push_back(((r - k) % n + n) % n);
+  }
+  return o;
+}
+
+// The order in which output shard r of n collects the ranks' partials.
+//   ring: r-1, r-2, ..., r (the accumulator travels {j -> j-1});
+//   unroll-by-2: chain r-1, r-3, ... then chain r-2, r-4, ... (two hops per iteration);
+//   bidirectional: r+a, ..., r+1 (left-moving), r-b, ..., r-1 (right-moving), then r itself,
+//   a = floor(n/2), b = floor((n-1)/2).
+std::vector<int> rs_order(int r, int n, int sched) {
+  auto md = [n](int v) { return ((v % n) + n) % n; };
+  std::vector<int> o;
+  if (sched == COCO_SCHED_RING) {
+    for (int i = 0; i < n; ++i) o.push_back(md(r - 1 - i));
+  } else if (sched == COCO_SCHED_UNROLL2) {
+    for (int i = 0; i < (n + 1) / 2; ++i) o.push_back(md(r - 1 - 2 * i));
+    for (int i = 0; i < n / 2; ++i) o.push_back(md(r - 2 - 2 * i));
+  } else {
+    const int a = n / 2, b = (n - 1) / 2;
+    for (int i = 0; i < a; ++i) o.push_back(md(r + a - i));
+    for (int i = 0; i < b; ++i) o.push_back(md(r - b + i));
+    o.push_back(r);
+  }
+  return o;
+}
+
+bool valid_schedule(int sched) { return sched >= COCO_SCHED_RING && sched <= COCO_SCHED_BIDIRECTIONAL; }
+
+coco_status looped_ag_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs, const coco_tensor* out,
+                             int sched, void* stream) {
+  if (!valid_schedule(sched)) return COCO_ERR_VALUE;
   EinsumArgs E;
   coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
   if (st != COCO_OK) return st;
@@ -668,14 +712,15 @@ COCO_EXPORT coco_status coco_looped_ag_einsum(const char* spec, const coco_tenso
     for (int r : output_ranks(E.out, g)) {
       const int oi = add_out(&P, make_out(E.out.ptr(g, r), o));
       const void* other = operand_ptr(Ot, g, r);
+      const std::vector<int> order = ag_order(r, n, sched);
       if (lab == 'k') {
-        // case 2: one job, N K-segments in ring order, Addition in TMEM.
+        // case 2: one job, N K-segments in schedule order, Addition in TMEM.
         Job J = make_job(oi, res);
         J.seg0 = static_cast<int16_t>(P.segs.size());
         J.nseg = static_cast<int16_t>(n);
         const int64_t ks = lhs_looped ? shard.c : shard.r;
         for (int i = 0; i < n; ++i) {
-          const int s = (r + i) % n;
+          const int s = order[i];
           const void* sp = Lp.ptr(g, s);
           int va, vb;
           if (lhs_looped) {  // DynamicSlice rows [s*ks, (s+1)*ks) of the local rhs
@@ -698,7 +743,7 @@ COCO_EXPORT coco_status coco_looped_ag_einsum(const char* spec, const coco_tenso
       } else {
         // cases 1 and 3: one job per step, DynamicUpdateSlice of shard s.
         for (int i = 0; i < n; ++i) {
-          const int s = (r + i) % n;
+          const int s = order[i];
           const void* sp = Lp.ptr(g, s);
           Dims3 ext = res;
           Job J = make_job(oi, ext);
@@ -733,8 +778,9 @@ COCO_EXPORT coco_status coco_looped_ag_einsum(const char* spec, const coco_tenso
   return finish(P, E, A.c, stream);
 }
 
-COCO_EXPORT coco_status coco_looped_einsum_rs(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
-                                              const coco_tensor* out, void* stream) {
+coco_status looped_einsum_rs(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs, const coco_tensor* out,
+                             int sched, void* stream) {
+  if (!valid_schedule(sched)) return COCO_ERR_VALUE;
   EinsumArgs E;
   coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
   if (st != COCO_OK) return st;
@@ -757,8 +803,9 @@ COCO_EXPORT coco_status coco_looped_einsum_rs(const char* spec, const coco_tenso
       Job J = make_job(add_out(&P, make_out(E.out.ptr(g, r), ol)), ol);
       J.seg0 = static_cast<int16_t>(P.segs.size());
       J.nseg = static_cast<int16_t>(n);
+      const std::vector<int> order = rs_order(r, n, sched);
       for (int i = 0; i < n; ++i) {
-        const int q = ((r - 1 - i) % n + n) % n;  // the ring order the accumulated shard r travels
+        const int q = order[i];  // the order in which the accumulated shard r collects partials
         Seg sg = make_seg(add_view(&P, make_view(E.lhs.ptr(g, q), a)), add_view(&P, make_view(E.rhs.ptr(g, q), b)),
                           a.c);
         if (olab == 'm') sg.a_r0 = static_cast<int32_t>(r * ol.r);  // DynamicSlice of lhs rows
@@ -769,4 +816,26 @@ COCO_EXPORT coco_status coco_looped_einsum_rs(const char* spec, const coco_tenso
     }
   }
   return finish(P, E, a.c, stream);
+}
+
+}  // namespace
+
+COCO_EXPORT coco_status coco_looped_ag_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                              const coco_tensor* out, void* stream) {
+  return looped_ag_einsum(spec, lhs, rhs, out, COCO_SCHED_RING, stream);
+}
+
+COCO_EXPORT coco_status coco_looped_ag_einsum_sched(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                                    const coco_tensor* out, int schedule, void* stream) {
+  return looped_ag_einsum(spec, lhs, rhs, out, schedule, stream);
+}
+
+COCO_EXPORT coco_status coco_looped_einsum_rs(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                              const coco_tensor* out, void* stream) {
+  return looped_einsum_rs(spec, lhs, rhs, out, COCO_SCHED_RING, stream);
+}
+
+COCO_EXPORT coco_status coco_looped_einsum_rs_sched(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                                    const coco_tensor* out, int schedule, void* stream) {
+  return looped_einsum_rs(spec, lhs, rhs, out, schedule, stream);
 }

@@ -251,6 +251,35 @@ coco_status coco_looped_ag_einsum(const char* spec, const coco_tensor* lhs, cons
 coco_status coco_looped_einsum_rs(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
                                   const coco_tensor* out, void* stream);
 
+/*
+ * Shard schedules of the Looped CollectiveEinsum ([Decomp] §5.4). They change
+ * only the order in which shards are visited (AllGather) or partials are
+ * collected (ReduceScatter), i.e. the fp32 accumulation order; the result is
+ * the same einsum.
+ *   COCO_SCHED_RING          §5.1: permutes {j -> j-1}. AllGather: rank r visits
+ *                            r, r+1, ..., r-1; ReduceScatter: output shard r
+ *                            collects ranks r-1, r-2, ..., r.
+ *   COCO_SCHED_UNROLL2       §5.4.1 (loop unrolled by 2): ReduceScatter as two
+ *                            interleaved chains travelling two hops per step,
+ *                            r-1, r-3, ... then r-2, r-4, ..., summed in an
+ *                            epilogue. On one GPU the AllGather order is the ring
+ *                            order (unrolling there only removes copies).
+ *   COCO_SCHED_BIDIRECTIONAL §5.4.2: shards / accumulators travel both ways.
+ *                            AllGather: r, r+1, r-1, r+2, r-2, ...;
+ *                            ReduceScatter: r+a, ..., r+1 (left-moving), then
+ *                            r-b, ..., r-1 (right-moving), then r itself, with
+ *                            a = floor(N/2), b = floor((N-1)/2).
+ */
+typedef enum { COCO_SCHED_RING = 0, COCO_SCHED_UNROLL2 = 1, COCO_SCHED_BIDIRECTIONAL = 2 } coco_schedule;
+
+/* coco_looped_ag_einsum with an explicit schedule (a coco_schedule value; others: COCO_ERR_VALUE). */
+coco_status coco_looped_ag_einsum_sched(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                        const coco_tensor* out, int schedule, void* stream);
+
+/* coco_looped_einsum_rs with an explicit schedule (a coco_schedule value; others: COCO_ERR_VALUE). */
+coco_status coco_looped_einsum_rs_sched(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                        const coco_tensor* out, int schedule, void* stream);
+
 /* ------------------------------------------------------------- utilities */
 
 /*

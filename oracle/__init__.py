@@ -41,8 +41,11 @@ from .einsum import einsum, einsum_bruteforce, parse_spec
 from .looped import (
     allgather_einsum,
     looped_allgather_einsum,
+    looped_allgather_einsum_bidirectional,
     einsum_reduce_scatter,
     looped_einsum_reduce_scatter,
+    looped_einsum_reduce_scatter_unrolled,
+    looped_einsum_reduce_scatter_bidirectional,
 )
 from .fused import (
     splitmix64,
@@ -64,8 +67,9 @@ __all__ = [
     "allgather", "reduce_scatter", "allreduce", "allreduce_split_rs_ag",
     "permute_pairs", "collective_permute",
     "einsum", "einsum_bruteforce", "parse_spec",
-    "allgather_einsum", "looped_allgather_einsum",
-    "einsum_reduce_scatter", "looped_einsum_reduce_scatter",
+    "allgather_einsum", "looped_allgather_einsum", "looped_allgather_einsum_bidirectional",
+    "einsum_reduce_scatter", "looped_einsum_reduce_scatter", "looped_einsum_reduce_scatter_unrolled",
+    "looped_einsum_reduce_scatter_bidirectional",
     "splitmix64", "counter_hash", "keep_threshold", "keep_mask", "dropout_scale",
     "fused_allreduce",
     "mlp_1d_forward", "mlp_1d_reference", "mlp_2d_forward", "mlp_2d_reference",

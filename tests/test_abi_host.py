@@ -199,3 +199,14 @@ def test_einsum_validation(coco):
     E = "coco_einsum"
     assert ein(coco, E, b"mk,kn->mn", lhs, rhs, out) == 4    # lhs sliced on m is not a local matmul
     assert ein(coco, E, b"mk,kn->mn", l2, r2, mk(coco, B16, R, (64, 16), 4, base=FAKE + (1 << 41))) == 4
+
+
+def test_schedule_validation(coco):
+    B16, L, S = coco.BF16, coco.LOCAL, coco.SLICED
+    lhs = mk(coco, B16, S, (64, 32), 4, slice_dim=0)
+    rhs = mk(coco, B16, L, (32, 16), 4, base=FAKE + (1 << 40))
+    out = mk(coco, B16, L, (64, 16), 4, base=FAKE + (1 << 41))
+    for name in ("coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched"):
+        for bad in (-1, 3, 99):
+            assert coco.raw_call(name, b"mk,kn->mn", ctypes.byref(lhs), ctypes.byref(rhs), ctypes.byref(out),
+                                 bad, None) == 10

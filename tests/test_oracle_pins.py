@@ -444,3 +444,64 @@ def test_planted_wrong_shard_index_in_case2_is_caught(monkeypatch):
     assert calls["k"] > 0
     assert any(not np.array_equal(x, y) for x, y in zip(good, bad))
     np.testing.assert_array_equal(good[0], oracle.einsum_bruteforce("mk,kn->mn", a_full, b_full))
+
+
+# ------------------------------------------- schedule variants ([Decomp] §5.4)
+
+
+@pytest.mark.parametrize("case", AG_CASES)
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8])
+def test_bidirectional_allgather_einsum_equals_monolithic(case, n):
+    spec, side, lab, shp, _ = case
+    shards = [small_ints(shp) for _ in range(n)]
+    locs = [small_ints(_other_shape(case, n)) for _ in range(n)]
+    trace = []
+    a = looped.looped_allgather_einsum_bidirectional(spec, side, lab, shards, locs, trace)
+    b = looped.allgather_einsum(spec, side, lab, shards, locs)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    # step k brings shards r+k and r-k (from the two directions); every shard is used once
+    for r in range(n):
+        used = [(st, s) for st, rr, s in trace if rr == r]
+        assert sorted(s for _, s in used) == list(range(n))
+        for st, s in used:
+            assert s in ((r + st) % n, (r - st) % n)
+    steps = {st for st, _, _ in trace}
+    assert len(steps) == n // 2 + 1  # about half the iterations of the ring form
+
+
+@pytest.mark.parametrize("out_label", ["m", "n"])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8])
+def test_unrolled_einsum_rs_equals_monolithic(out_label, n):
+    lhs = [small_ints((2 * n, 3)) for _ in range(n)]
+    rhs = [small_ints((3, 2 * n)) for _ in range(n)]
+    trace = []
+    a = looped.looped_einsum_reduce_scatter_unrolled("mk,kn->mn", lhs, rhs, out_label, trace)
+    b = looped.einsum_reduce_scatter("mk,kn->mn", lhs, rhs, out_label)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    # two interleaved chains: A collects ranks r-1, r-3, ..., B ranks r-2, r-4, ...
+    for r in range(n):
+        ca = [q for i, q, c, s in sorted(trace) if s == r and c == "A"]
+        cb = [q for i, q, c, s in sorted(trace) if s == r and c == "B"]
+        assert ca == [(r - 1 - 2 * i) % n for i in range(len(ca))]
+        assert cb == [(r - 2 - 2 * i) % n for i in range(len(cb))]
+        assert sorted(ca + cb) == list(range(n))
+
+
+@pytest.mark.parametrize("out_label", ["m", "n"])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8])
+def test_bidirectional_einsum_rs_equals_monolithic(out_label, n):
+    lhs = [small_ints((2 * n, 3)) for _ in range(n)]
+    rhs = [small_ints((3, 2 * n)) for _ in range(n)]
+    trace = []
+    a = looped.looped_einsum_reduce_scatter_bidirectional("mk,kn->mn", lhs, rhs, out_label, trace)
+    b = looped.einsum_reduce_scatter("mk,kn->mn", lhs, rhs, out_label)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    for r in range(n):
+        left = [q for i, q, d, s in sorted(trace) if s == r and d == "left"]
+        right = [q for i, q, d, s in sorted(trace) if s == r and d == "right"]
+        assert left == [(r + len(left) - i) % n for i in range(len(left))]  # r+a, ..., r+1
+        assert right == [(r - len(right) + i) % n for i in range(len(right))]  # r-b, ..., r-1
+        assert abs(len(left) - len(right)) <= 1 and len(left) + len(right) == n - 1
