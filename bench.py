@@ -528,8 +528,78 @@ class RsAg(Workload):
         return self.numel // 4096
 
 
+def bert_large_parameter_shapes():
+    """Parameter shapes of BERT-large (hidden 1024, 24 layers, FFN 4096, 30522-token vocabulary,
+    512 positions): about 335 M elements, the size the scattered-tensor section quotes for BERT."""
+    h, ffn, layers = 1024, 4096, 24
+    shapes = [(30522, h), (512, h), (2, h), (h,), (h,)]
+    for _ in range(layers):
+        for _ in range(4):  # query, key, value, attention output
+            shapes += [(h, h), (h,)]
+        shapes += [(h,), (h,), (h, ffn), (ffn,), (ffn, h), (h,), (h,), (h,)]
+    shapes += [(h, h), (h,)]  # pooler
+    return shapes
+
+
+class ScatteredGradients(Workload):
+    """Data-parallel gradient AllReduce over BERT-large's separately allocated parameter
+    tensors, 8 ranks, fp16, in place, averaged (alpha = 1/8)."""
+
+    name = "scattered_allreduce"
+    dtype = "f16"
+
+    def __init__(self, dev, n=8, cfg=6):
+        from collective_fusedallreduce_gb300 import coco
+        self.n = n
+        self.shapes = bert_large_parameter_shapes()
+        self.grads = [[gen(dev, 100000 * cfg + 1000 * r + t, s, torch.float16, 1e-3) for t, s in enumerate(self.shapes)]
+                      for r in range(n)]
+        self.numel = sum(int(np.prod(s)) for s in self.shapes)
+        nbytes = coco.coco_scattered_table_bytes([int(np.prod(s)) for s in self.shapes], n)
+        self.table = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.plan = coco.coco_scattered_table_build(self.grads, self.table)
+        self.config = {"workload": f"scattered-tensor AllReduce (CoCoNet): BERT-large parameter list, "
+                                   f"{len(self.shapes)} tensors, {self.numel} elements per rank, 8 ranks, fp16, in place, "
+                                   f"averaged", "ranks": n, "tensors": len(self.shapes), "elements_per_rank": self.numel,
+                       "bucket_table_bytes": nbytes, "l2": "no flush: each step moves 10.7 GB"}
+
+    def kernels(self):
+        b = self.numel * 2
+        return [("k_scattered_allreduce (1024-element buckets, round-robin over warps)", "hbm",
+                 2 * self.n * b + 12 * self.plan.nbuckets * self.n, 1)]
+
+    def step(self, stream, marks=None):
+        from collective_fusedallreduce_gb300 import coco
+        if marks:
+            marks[0].record(stream)
+        coco.coco_scattered_allreduce(self.plan, 1.0 / self.n, stream)
+        if marks:
+            marks[1].record(stream)
+
+    def host_inputs(self):
+        return [(t, t.cpu().pin_memory()) for row in self.grads for t in row], self.grads[0][0]
+
+    def oracle_sample(self, rows):
+        import oracle
+        from collective_fusedallreduce_gb300 import synth
+        # a sample of whole tensors, in list order, up to `rows` * 4096 elements
+        picked, total = [], 0
+        for t, s in enumerate(self.shapes):
+            if total >= rows * 4096:
+                break
+            picked.append(t)
+            total += int(np.prod(s))
+        per_rank = [[synth.as_f64(self.grads[r][t]) for t in picked] for r in range(self.n)]
+        t0 = time.perf_counter()
+        oracle.scattered_allreduce(per_rank, 1.0 / self.n)
+        return time.perf_counter() - t0, total / self.numel
+
+    def full_sample(self):
+        return self.numel // 4096
+
+
 WORKLOADS = {"c2": MegatronTail, "c2f": MegatronTailFused, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
-             "c5b": RsAg}
+             "c5b": RsAg, "scatter": ScatteredGradients}
 
 
 # --------------------------------------------------------------- helpers

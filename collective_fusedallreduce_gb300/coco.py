@@ -52,6 +52,11 @@ class CocoTensor(ctypes.Structure):
     ]
 
 
+class CocoScatteredPlan(ctypes.Structure):
+    _fields_ = [("table", ctypes.c_void_p), ("nbuckets", ctypes.c_int64), ("nranks", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
 class CocoError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
@@ -84,6 +89,14 @@ for _name, _args in {
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int
+_lib.coco_scattered_table_bytes.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]
+_lib.coco_scattered_table_bytes.restype = ctypes.c_size_t
+_lib.coco_scattered_table_build.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p,
+                                            ctypes.c_size_t, ctypes.POINTER(CocoScatteredPlan), _S]
+_lib.coco_scattered_table_build.restype = ctypes.c_int
+_lib.coco_scattered_allreduce.argtypes = [ctypes.POINTER(CocoScatteredPlan), ctypes.c_float, _S]
+_lib.coco_scattered_allreduce.restype = ctypes.c_int
 _lib.coco_status_string.argtypes = [ctypes.c_int]
 _lib.coco_status_string.restype = ctypes.c_char_p
 _lib.coco_last_cuda_error.restype = ctypes.c_int
@@ -95,6 +108,7 @@ EXPORTED = [
     "coco_allreduce_rs_ag_noalloc",
     "coco_einsum", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs",
     "coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched", "coco_dropout_keep_mask",
+    "coco_scattered_table_bytes", "coco_scattered_table_build", "coco_scattered_allreduce",
     "coco_device_status", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
 ]
 
@@ -249,3 +263,28 @@ def raw_call(name, *args):
     """Calls a C entry point with already-marshalled ctypes arguments and
     returns its status code (used by the interface tests)."""
     return getattr(_lib, name)(*args)
+
+
+def coco_scattered_table_bytes(numels, nranks):
+    arr = (ctypes.c_int64 * len(numels))(*[int(n) for n in numels])
+    return int(_lib.coco_scattered_table_bytes(len(numels), arr, int(nranks)))
+
+
+def coco_scattered_table_build(per_rank, table, stream=None):
+    """``per_rank[r][t]``: rank r's tensor t (same sizes and dtype on every rank);
+    ``table``: a device uint8 tensor of at least coco_scattered_table_bytes() bytes.
+    Returns the plan for coco_scattered_allreduce."""
+    nranks, ntensors = len(per_rank), len(per_rank[0])
+    numels = (ctypes.c_int64 * ntensors)(*[x.numel() for x in per_rank[0]])
+    ptrs = (ctypes.c_void_p * (nranks * ntensors))(*[x.data_ptr() if x.numel() else None
+                                                     for row in per_rank for x in row])
+    plan = CocoScatteredPlan()
+    dtype = _DTYPES[per_rank[0][0].dtype] if ntensors else F32
+    _check(_lib.coco_scattered_table_build(ntensors, numels, dtype, nranks, ptrs, ctypes.c_void_p(table.data_ptr()),
+                                           table.numel() * table.element_size(), ctypes.byref(plan), _stream(stream)),
+           "coco_scattered_table_build")
+    return plan
+
+
+def coco_scattered_allreduce(plan, alpha=1.0, stream=None):
+    _check(_lib.coco_scattered_allreduce(ctypes.byref(plan), float(alpha), _stream(stream)), "coco_scattered_allreduce")

@@ -9,6 +9,7 @@
 // Computation via Decomposition in Large Deep Learning Models", §5.1.
 
 #include <atomic>
+#include <algorithm>
 #include <set>
 #include <cmath>
 #include <cstring>
@@ -467,6 +468,96 @@ COCO_EXPORT coco_status coco_allreduce_rs_ag(const coco_tensor* in, const coco_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((st = cuda_status(launch_reduce_scatter(rs, s))) != COCO_OK) return st;
   return cuda_status(launch_allgather(ag, s));
+}
+
+// ------------------------------------------------------- scattered tensors
+
+namespace {
+constexpr uint32_t kScatterMagic = 0x5343544Bu;  // table header tag
+constexpr int kScatterHeaderBytes = 64;
+
+int64_t scatter_buckets(int32_t ntensors, const int64_t* numels) {
+  int64_t nb = 0;
+  for (int32_t t = 0; t < ntensors; ++t) nb += (numels[t] + 1023) / 1024;
+  return nb;
+}
+}  // namespace
+
+COCO_EXPORT size_t coco_scattered_table_bytes(int32_t ntensors, const int64_t* numels, int32_t nranks) {
+  if (ntensors < 0 || nranks < 1 || (ntensors > 0 && !numels)) return 0;
+  for (int32_t t = 0; t < ntensors; ++t)
+    if (numels[t] < 0) return 0;
+  return static_cast<size_t>(kScatterHeaderBytes) +
+         static_cast<size_t>(12) * static_cast<size_t>(scatter_buckets(ntensors, numels)) * nranks;
+}
+
+COCO_EXPORT coco_status coco_scattered_table_build(int32_t ntensors, const int64_t* numels, int32_t dtype,
+                                                   int32_t nranks, void* const* tensors, void* table,
+                                                   size_t table_bytes, coco_scattered_plan* plan, void* stream) {
+  if (!plan) return COCO_ERR_NULL;
+  if (ntensors < 0 || nranks < 1 || nranks > COCO_MAX_PTRS) return COCO_ERR_SHAPE;
+  if (ntensors > 0 && (!numels || !tensors)) return COCO_ERR_NULL;
+  if (dtype < COCO_F32 || dtype > COCO_BF16) return COCO_ERR_DTYPE;
+  for (int32_t t = 0; t < ntensors; ++t)
+    if (numels[t] < 0 || numels[t] >= (int64_t(1) << 32)) return COCO_ERR_SHAPE;
+  const int64_t nb = scatter_buckets(ntensors, numels);
+  const size_t need = coco_scattered_table_bytes(ntensors, numels, nranks);
+  if (!table) return COCO_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(table) & 15) return COCO_ERR_ALIGN;
+  if (table_bytes < need) return COCO_ERR_SHAPE;
+  const int es = dtype_size(dtype);
+  std::vector<Range> ranges;
+  for (int32_t r = 0; r < nranks; ++r)
+    for (int32_t t = 0; t < ntensors; ++t) {
+      if (numels[t] == 0) continue;
+      const void* p = tensors[static_cast<size_t>(r) * ntensors + t];
+      if (!p) return COCO_ERR_NULL;
+      if (reinterpret_cast<uintptr_t>(p) & 15) return COCO_ERR_ALIGN;
+      ranges.push_back(range_of(p, numels[t] * es));
+    }
+  ranges.push_back(range_of(table, static_cast<int64_t>(need)));
+  std::sort(ranges.begin(), ranges.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+  for (size_t i = 1; i < ranges.size(); ++i)
+    if (ranges[i].lo < ranges[i - 1].hi) return COCO_ERR_ALIAS;
+
+  std::vector<uint32_t> words(need / 4, 0u);
+  words[0] = kScatterMagic;
+  words[1] = static_cast<uint32_t>(nb & 0xFFFFFFFFu);
+  words[2] = static_cast<uint32_t>(nb >> 32);
+  words[3] = static_cast<uint32_t>(nranks);
+  words[4] = static_cast<uint32_t>(dtype);
+  words[5] = static_cast<uint32_t>(ntensors);
+  size_t w = kScatterHeaderBytes / 4;
+  for (int32_t t = 0; t < ntensors; ++t) {
+    for (int64_t off = 0, bi = 0; off < numels[t]; off += 1024, ++bi) {
+      const int64_t len = std::min<int64_t>(1024, numels[t] - off);
+      const uint32_t code = static_cast<uint32_t>(bi << 10) | static_cast<uint32_t>(len - 1);
+      for (int32_t r = 0; r < nranks; ++r) {
+        const uint64_t a = reinterpret_cast<uint64_t>(tensors[static_cast<size_t>(r) * ntensors + t]);
+        words[w++] = static_cast<uint32_t>(a & 0xFFFFFFFFu);
+        words[w++] = static_cast<uint32_t>(a >> 32);
+        words[w++] = code;
+      }
+    }
+  }
+  plan->table = table;
+  plan->nbuckets = nb;
+  plan->nranks = nranks;
+  plan->dtype = dtype;
+  // pageable source: the runtime stages it before returning, so `words` may go out of scope
+  return cuda_status(cudaMemcpyAsync(table, words.data(), need, cudaMemcpyHostToDevice, static_cast<cudaStream_t>(stream)));
+}
+
+COCO_EXPORT coco_status coco_scattered_allreduce(const coco_scattered_plan* plan, float alpha, void* stream) {
+  if (!plan) return COCO_ERR_NULL;
+  if (plan->nbuckets < 0 || plan->nranks < 1 || plan->nranks > COCO_MAX_PTRS) return COCO_ERR_SHAPE;
+  if (plan->dtype < COCO_F32 || plan->dtype > COCO_BF16) return COCO_ERR_DTYPE;
+  if (!(alpha == alpha)) return COCO_ERR_VALUE;
+  if (plan->nbuckets == 0) return COCO_OK;
+  if (!plan->table) return COCO_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(plan->table) & 15) return COCO_ERR_ALIGN;
+  return cuda_status(launch_scattered_allreduce(plan->table, plan->nbuckets, plan->nranks, plan->dtype, alpha,
+                                                static_cast<cudaStream_t>(stream)));
 }
 
 COCO_EXPORT coco_status coco_dropout_keep_mask(uint64_t seed, float dropout_p, uint64_t first_index, uint64_t count,

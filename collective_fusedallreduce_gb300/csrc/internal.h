@@ -53,6 +53,11 @@ struct SliceLaunch {
 cudaError_t launch_reduce_scatter(const SliceLaunch& L, cudaStream_t s);
 cudaError_t launch_allgather(const SliceLaunch& L, cudaStream_t s);
 
+// Scattered-tensor AllReduce over a device bucket table (header of 16 words,
+// then 3 words per (bucket, rank) entry).
+cudaError_t launch_scattered_allreduce(const void* table, int64_t nbuckets, int nranks, int dtype, float alpha,
+                                       cudaStream_t s);
+
 cudaError_t launch_keep_mask(uint64_t seed, uint32_t threshold, uint64_t first, uint64_t count,
                              uint8_t* mask, cudaStream_t s);
 

@@ -311,6 +311,78 @@ __global__ void __launch_bounds__(kThreads) k_allgather(const __grid_constant__ 
   }
 }
 
+// -------------------------------------------------------- scattered tensors
+//
+// [CoCoNet], scattered tensors: buckets of at most 1024 elements, taken by
+// warps round-robin; a warp reads its bucket's N entries (address, offset) and
+// reduces the bucket across ranks with 16-byte vectors (scalar tail for the
+// last bucket of a tensor), writing the result back to every rank in place.
+
+constexpr int kScatterHeaderWords = 16;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_scattered_allreduce(const uint32_t* __restrict__ table, int64_t nbuckets,
+                                                                  int nranks, float alpha) {
+  using V = V16<T>;
+  constexpr int VE = V::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * kThreads) >> 5;
+  const uint32_t* entries = table + kScatterHeaderWords;
+  for (int64_t b = warp; b < nbuckets; b += nwarps) {
+    const uint32_t* e = entries + b * nranks * 3;
+    const uint32_t off = e[2];  // the same bucket offset and length for every rank
+    const int len = static_cast<int>(off & 1023u) + 1;
+    const int64_t first = static_cast<int64_t>(off >> 10) * 1024;
+    const int nvec = len / VE;
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[VE];
+      for (int r0 = 0; r0 < nranks; r0 += 8) {
+        uint4 raw[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r0 + r < nranks) {
+            const uint32_t* er = e + 3 * (r0 + r);
+            const char* base = reinterpret_cast<const char*>((static_cast<uint64_t>(er[1]) << 32) | er[0]);
+            raw[r] = ld_stream(base + (first + static_cast<int64_t>(v) * VE) * sizeof(T));
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          if (r0 + r < nranks) {
+            float f[VE];
+            V::load(raw[r], f);
+#pragma unroll
+            for (int j = 0; j < VE; ++j) acc[j] = (r0 + r == 0) ? f[j] : acc[j] + f[j];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < VE; ++j) acc[j] *= alpha;
+      const uint4 o = V::store(acc);
+      for (int r = 0; r < nranks; ++r) {
+        const uint32_t* er = e + 3 * r;
+        char* base = reinterpret_cast<char*>((static_cast<uint64_t>(er[1]) << 32) | er[0]);
+        st_vec(base + (first + static_cast<int64_t>(v) * VE) * sizeof(T), o);
+      }
+    }
+    for (int i = nvec * VE + lane; i < len; i += 32) {  // tail of a tensor's last bucket
+      float acc = 0.0f;
+      for (int r = 0; r < nranks; ++r) {
+        const uint32_t* er = e + 3 * r;
+        const T* base = reinterpret_cast<const T*>((static_cast<uint64_t>(er[1]) << 32) | er[0]);
+        acc = (r == 0) ? static_cast<float>(base[first + i]) : acc + static_cast<float>(base[first + i]);
+      }
+      acc *= alpha;
+      for (int r = 0; r < nranks; ++r) {
+        const uint32_t* er = e + 3 * r;
+        T* base = reinterpret_cast<T*>((static_cast<uint64_t>(er[1]) << 32) | er[0]);
+        base[first + i] = static_cast<T>(acc);
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ mask
 
 __global__ void k_keep_mask(uint64_t seed, uint32_t threshold, uint64_t first, uint64_t count, uint8_t* mask) {
@@ -418,6 +490,19 @@ cudaError_t launch_allgather(const SliceLaunch& L, cudaStream_t s) {
   const SliceArgs a = slice_args(L);
   dim3 grid(grid_for(a.outer * a.chunk_vecs, kThreads * kUnroll), L.ngroups * L.nranks);
   k_allgather<<<grid, kThreads, 0, s>>>(a);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scattered_allreduce(const void* table, int64_t nbuckets, int nranks, int dtype, float alpha,
+                                       cudaStream_t s) {
+  const int grid = grid_for(nbuckets * 32, kThreads);  // one warp per bucket until the grid is full
+  const uint32_t* t = static_cast<const uint32_t*>(table);
+  switch (dtype) {
+    case COCO_F32: k_scattered_allreduce<float><<<grid, kThreads, 0, s>>>(t, nbuckets, nranks, alpha); break;
+    case COCO_F16: k_scattered_allreduce<__half><<<grid, kThreads, 0, s>>>(t, nbuckets, nranks, alpha); break;
+    default: k_scattered_allreduce<__nv_bfloat16><<<grid, kThreads, 0, s>>>(t, nbuckets, nranks, alpha); break;
+  }
   count_launch();
   return cudaGetLastError();
 }

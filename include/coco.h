@@ -176,6 +176,52 @@ coco_status coco_allreduce_rs_ag(const coco_tensor* in, const coco_tensor* scrat
  */
 coco_status coco_allreduce_rs_ag_noalloc(const coco_tensor* in, const coco_tensor* out, void* stream);
 
+/* ------------------------------------------------------ scattered tensors */
+
+/*
+ * AllReduce of scattered tensors ([CoCoNet], the section on scattered
+ * tensors): the gradients of data parallelism live in many separate buffers;
+ * one kernel reduces all of them without first copying them into one buffer.
+ * Each tensor is cut into buckets of at most 1024 elements, and each bucket is
+ * described per rank by 12 bytes: the 64-bit address of the rank's tensor and
+ * a 32-bit offset. Warps take buckets round-robin.
+ *
+ * The bucket table is built once (the same tensors are reduced every training
+ * step) into caller-owned device memory of coco_scattered_table_bytes() bytes:
+ * a 64-byte header, then nbuckets * nranks entries of 12 bytes, rank-inner. An
+ * entry's 32-bit offset holds the bucket index within its tensor in bits
+ * 10..31 (the element offset is that index * 1024) and the bucket length - 1
+ * in bits 0..9.
+ */
+typedef struct {
+  void* table;       /* device table (caller's memory) */
+  int64_t nbuckets;  /* buckets over all tensors */
+  int32_t nranks;
+  int32_t dtype;     /* coco_dtype of every tensor */
+} coco_scattered_plan;
+
+/* Bytes of device memory the table of these tensors needs (64 + 12 * nbuckets * nranks). */
+size_t coco_scattered_table_bytes(int32_t ntensors, const int64_t* numels, int32_t nranks);
+
+/*
+ * Builds the table into `table` (device, 16-byte aligned, at least
+ * coco_scattered_table_bytes() bytes; a host-to-device copy ordered on
+ * `stream`) and fills `plan`. `tensors[r * ntensors + t]` is rank r's tensor t
+ * (device pointer, 16-byte aligned, numels[t] elements of `dtype`, dense);
+ * numels[t] < 2^32. Tensors may not overlap each other or the table
+ * (COCO_ERR_ALIAS).
+ */
+coco_status coco_scattered_table_build(int32_t ntensors, const int64_t* numels, int32_t dtype, int32_t nranks,
+                                       void* const* tensors, void* table, size_t table_bytes,
+                                       coco_scattered_plan* plan, void* stream);
+
+/*
+ * In place on every rank: tensor_r[t][e] = alpha * sum_{q=0}^{N-1} tensor_q[t][e]
+ * for every tensor t, with the sum and the scale in fp32 (rank order 0..N-1)
+ * and one rounding; alpha = 1 is the plain AllReduce, 1/N averages.
+ */
+coco_status coco_scattered_allreduce(const coco_scattered_plan* plan, float alpha, void* stream);
+
 /* ---------------------------------------------------------------- einsums */
 
 /*

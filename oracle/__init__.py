@@ -55,6 +55,12 @@ from .fused import (
     dropout_scale,
     fused_allreduce,
 )
+from .scattered import (
+    buckets as scattered_buckets,
+    metadata_bytes as scattered_metadata_bytes,
+    scattered_allreduce,
+    scattered_allreduce_by_buckets,
+)
 from .mlp import (
     mlp_1d_forward,
     mlp_1d_reference,
@@ -74,4 +80,5 @@ __all__ = [
     "fused_allreduce",
     "mlp_1d_forward", "mlp_1d_reference", "mlp_2d_forward", "mlp_2d_reference",
     "megatron_attention_tail",
+    "scattered_buckets", "scattered_metadata_bytes", "scattered_allreduce", "scattered_allreduce_by_buckets",
 ]

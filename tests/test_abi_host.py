@@ -210,3 +210,32 @@ def test_schedule_validation(coco):
         for bad in (-1, 3, 99):
             assert coco.raw_call(name, b"mk,kn->mn", ctypes.byref(lhs), ctypes.byref(rhs), ctypes.byref(out),
                                  bad, None) == 10
+
+
+def test_scattered_table_validation(coco):
+    assert coco.coco_scattered_table_bytes([0], 4) == 64
+    assert coco.coco_scattered_table_bytes([1024, 1025, 1], 8) == 64 + 12 * (1 + 2 + 1) * 8
+    assert coco.coco_scattered_table_bytes([-1], 2) == 0
+    lib = coco._lib
+    numels = (ctypes.c_int64 * 2)(1000, 3000)
+    plan = coco.CocoScatteredPlan()
+    def build(ptrs, table=FAKE + (1 << 44), tbytes=1 << 20, dtype=coco.F16, nranks=2, nums=numels):
+        arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+        return lib.coco_scattered_table_build(2, nums, dtype, nranks, arr, ctypes.c_void_p(table), tbytes,
+                                              ctypes.byref(plan), None)
+    good = [FAKE + i * (1 << 32) for i in range(4)]
+    assert build(good, dtype=9) == 3
+    assert build(good, nranks=0) == 2
+    assert build([good[0], 0, good[2], good[3]]) == 1
+    assert build([good[0] + 8] + good[1:]) == 5
+    assert build(good, table=FAKE + (1 << 44) + 4) == 5
+    assert build(good, tbytes=100) == 2
+    assert build([good[0], good[0] + 64] + good[2:]) == 6          # overlapping tensors
+    assert build(good, table=good[1] + 256) == 6                   # table inside a tensor
+    big = (ctypes.c_int64 * 2)(1 << 32, 1)
+    assert build(good, nums=big) == 2
+    assert lib.coco_scattered_allreduce(None, ctypes.c_float(1.0), None) == 1
+    p2 = coco.CocoScatteredPlan(None, 0, 2, coco.F16)
+    assert lib.coco_scattered_allreduce(ctypes.byref(p2), ctypes.c_float(1.0), None) == 0  # nothing to do
+    p3 = coco.CocoScatteredPlan(None, 5, 2, coco.F16)
+    assert lib.coco_scattered_allreduce(ctypes.byref(p3), ctypes.c_float(1.0), None) == 1

@@ -505,3 +505,41 @@ def test_bidirectional_einsum_rs_equals_monolithic(out_label, n):
         assert left == [(r + len(left) - i) % n for i in range(len(left))]  # r+a, ..., r+1
         assert right == [(r - len(right) + i) % n for i in range(len(right))]  # r-b, ..., r-1
         assert abs(len(left) - len(right)) <= 1 and len(left) + len(right) == n - 1
+
+
+# ----------------------------------------------------- scattered tensors ([CoCoNet])
+
+
+def test_scattered_metadata_matches_the_page():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "scattered_metadata.txt")) if l.strip() and not l.startswith("#")]
+    for elements, percent in rows:
+        meta = oracle.scattered_metadata_bytes(int(elements))
+        assert meta == 12 * -(-int(elements) // 1024)
+        # as a share of the model's 16-bit storage, rounded as the page prints it
+        assert round(100.0 * meta / (2 * int(elements)), 1) == float(percent)
+
+
+@pytest.mark.parametrize("numels", [[0], [1], [1023, 1024, 1025], [5000, 1, 0, 2048]])
+def test_scattered_buckets_cover_every_element_once(numels):
+    bl = oracle.scattered_buckets(numels)
+    assert all(0 < ln <= 1024 for _, _, ln in bl)
+    for t, n in enumerate(numels):
+        mine = [(off, ln) for tt, off, ln in bl if tt == t]
+        assert len(mine) == -(-n // 1024)
+        covered = sorted(i for off, ln in mine for i in range(off, off + ln))
+        assert covered == list(range(n))
+        assert sum(1 for _ in mine) * 12 == oracle.scattered_metadata_bytes(n)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 8])
+def test_scattered_allreduce_closed_form_and_bucket_walk(n):
+    shapes = [(3, 5), (1,), (2050,), (4, 300)]
+    per_rank = [[np.full(s, float(r + 1)) for s in shapes] for r in range(n)]
+    out = oracle.scattered_allreduce(per_rank, alpha=0.5)
+    for o, s in zip(out, shapes):
+        assert o.shape == s and np.all(o == 0.5 * n * (n + 1) / 2)
+    rnd = [[RNG.standard_normal(s) for s in shapes] for _ in range(n)]
+    a = oracle.scattered_allreduce(rnd, 0.25)
+    b = oracle.scattered_allreduce_by_buckets(rnd, 0.25)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
