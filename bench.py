@@ -487,14 +487,16 @@ class RsAg(Workload):
     name = "allreduce_split_rs_ag"
     dtype = "f32"
 
-    def __init__(self, dev, n=8, numel=1 << 28, cfg=5):
+    def __init__(self, dev, n=8, numel=1 << 28, cfg=5, small=False):
         from collective_fusedallreduce_gb300 import synth
+        numel = numel >> 3 if small else numel
         self.n, self.numel = n, numel
         self.inp = [gen(dev, synth.seed_of(cfg, 5, r), (numel,), torch.float32, kind="uniform") for r in range(n)]
         self.scratch = [torch.empty(numel // n, device=dev) for _ in range(n)]
         self.out = [torch.empty(numel, device=dev) for _ in range(n)]
-        self.config = {"workload": "AllReduce split RS-AG, N=8 fp32, 2^28 elements (1 GiB) per rank, 8 distinct "
-                                   "outputs", "ranks": n, "l2": "no flush: each step moves 18 GiB"}
+        self.config = {"workload": f"AllReduce split RS-AG, N=8 fp32, {numel} elements ({numel * 4 >> 20} MiB) per "
+                                   f"rank, 8 distinct outputs", "ranks": n,
+                       "l2": f"no flush: each step moves {18 * numel * 4 >> 30} GiB"}
 
     def kernels(self):
         b = self.numel * 4
@@ -528,10 +530,10 @@ class RsAg(Workload):
         return self.numel // 4096
 
 
-def bert_large_parameter_shapes():
+def bert_large_parameter_shapes(layers=24):
     """Parameter shapes of BERT-large (hidden 1024, 24 layers, FFN 4096, 30522-token vocabulary,
     512 positions): about 335 M elements, the size the scattered-tensor section quotes for BERT."""
-    h, ffn, layers = 1024, 4096, 24
+    h, ffn = 1024, 4096
     shapes = [(30522, h), (512, h), (2, h), (h,), (h,)]
     for _ in range(layers):
         for _ in range(4):  # query, key, value, attention output
@@ -548,10 +550,10 @@ class ScatteredGradients(Workload):
     name = "scattered_allreduce"
     dtype = "f16"
 
-    def __init__(self, dev, n=8, cfg=6):
+    def __init__(self, dev, n=8, cfg=6, small=False):
         from collective_fusedallreduce_gb300 import coco
         self.n = n
-        self.shapes = bert_large_parameter_shapes()
+        self.shapes = bert_large_parameter_shapes(6 if small else 24)
         self.grads = [[gen(dev, 100000 * cfg + 1000 * r + t, s, torch.float16, 1e-3) for t, s in enumerate(self.shapes)]
                       for r in range(n)]
         self.numel = sum(int(np.prod(s)) for s in self.shapes)
@@ -727,6 +729,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
+    ap.add_argument("--small", action="store_true",
+                    help="reduced size of the c5b and scatter workloads (a few GB on the device, for ncu)")
     args = ap.parse_args()
     peaks = load_peaks()
 
@@ -752,7 +756,7 @@ def main():
         dist.barrier()
     from collective_fusedallreduce_gb300 import coco
 
-    wl = WORKLOADS[args.workload](dev)
+    wl = WORKLOADS[args.workload](dev, **({"small": True} if args.small and args.workload in ("c5b", "scatter") else {}))
     stream = torch.cuda.current_stream(dev)
     kern = wl.timed()
     nk = len(kern)
