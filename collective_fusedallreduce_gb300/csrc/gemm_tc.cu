@@ -43,21 +43,29 @@ constexpr int B_BYTES = B_BOX_BYTES * (BN / 64);  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
 constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 B
 
-// Shared-memory budget per epilogue mode: a 4-stage operand ring and four
-// epilogue warps (one per TMEM lane quarter). Eight epilogue warps (two per
-// quarter, each taking half of the columns) fit only with three stages; the
-// MMA warp does not wait on the epilogue in either mode, so four stages win.
-template <int MODE>
+// Shared-memory budget. ONE CTA PER MMA (TWO_SM = false): each CTA of a pair
+// receives the whole B tile (its own half plus the peer's, multicast), 48 KB
+// per stage, 4 stages. TWO_SM: the pair runs one M=256 MMA over both CTAs'
+// shared memory (tcgen05 cta_group::2), each CTA holding its own A tile and
+// its own 128-column half of B, 32 KB per stage, 6 stages. Four epilogue
+// warps (one per TMEM lane quarter) in both.
+template <int MODE, bool TWO_SM>
 struct Cfg {
-  static constexpr int STAGES = 4;
+  static constexpr int B_STAGE = TWO_SM ? B_BYTES / 2 : B_BYTES;
+  static constexpr int STAGE = A_BYTES + B_STAGE;
+  static constexpr int STAGES = TWO_SM ? 6 : 4;
   static constexpr int EPI_WARPS = 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr int EPI_OFF = STAGES * STAGE;
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_STRIP;  // two strips per epilogue warp
   static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 };
+// The pair MMA needs fewer operand bytes per SM and a deeper ring, which pays
+// when tiles have long K loops (operand-bound); with short ones the epilogue
+// dominates and the two CTAs are better left independent.
+constexpr int kTwoSmMinKBlocks = 4;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int GROUP_M = 16;  // tile rasterisation: 16 m-tiles per group, n-major inside
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -169,6 +177,25 @@ __device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtens
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "h"(cta_mask), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// The shared::cluster address of the same shared-memory offset in CTA 0 of the cluster.
+__device__ __forceinline__ uint32_t mapa_rank0(uint32_t addr) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(addr));
+  return r;
+}
+// A tile copy into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (cta_group::2).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -181,13 +208,25 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// TMEM allocation; for the pair (cta_group::2) one warp in each of the two CTAs executes it.
+template <bool PAIR>
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (PAIR) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
 }
+template <bool PAIR>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  if constexpr (PAIR)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 or f16 in, fp32 accumulate).
@@ -204,6 +243,24 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+// D[tmem of both CTAs] (+)= A[both CTAs' smem] * B[both CTAs' smem]: one M=256 MMA of the pair
+// (each CTA holds 128 rows of A, 128 columns of B and its 128 rows of D), issued by CTA 0.
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier at offset `bar` of every CTA in `cta_mask` once the pair's MMAs issued so far are done.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 // The same, arriving on the mbarrier at offset `bar` of every CTA in `cta_mask`.
 __device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
@@ -351,11 +408,12 @@ __device__ __forceinline__ bool keep_state(uint64_t z, uint32_t threshold) {
 // add the bias, apply dropout and add the residual in registers, then store
 // the tile to every replica of the group ([CoCoNet] §5.2, FusedAllReduce,
 // with the MatMul of its Fig. 3 fused in front).
-template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 1)
+template <int MODE, bool TWO_SM>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::THREADS, 1)
     k_gemm_tc(const __grid_constant__ TcParams P) {
-  constexpr int STAGES = Cfg<MODE>::STAGES, EPI_WARPS = Cfg<MODE>::EPI_WARPS;
-  constexpr int EPI_OFF = Cfg<MODE>::EPI_OFF, BAR_OFF = Cfg<MODE>::BAR_OFF, NUM_BARS = Cfg<MODE>::NUM_BARS;
+  using C = Cfg<MODE, TWO_SM>;
+  constexpr int STAGES = C::STAGES, EPI_WARPS = C::EPI_WARPS, STAGE_BYTES = C::STAGE;
+  constexpr int EPI_OFF = C::EPI_OFF, BAR_OFF = C::BAR_OFF, NUM_BARS = C::NUM_BARS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -379,17 +437,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 2);  // freed when both CTAs' MMAs have read the stage
+      // one CTA per MMA: freed when both CTAs' MMAs have read the stage; pair MMA: by CTA 0's commit
+      mbar_init(empty_bar(s), TWO_SM ? 1 : 2);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 32 * EPI_WARPS);
+      // one arrival per epilogue warp; pair MMA: CTA 0's accumulator is free once both CTAs'
+      // epilogues have read their halves
+      mbar_init(tempty_bar(a), (TWO_SM ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 1) tmem_alloc<TWO_SM>(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
   cluster_sync();  // the peer's barriers exist before anything is multicast into them
   tc_fence_after();
@@ -423,19 +484,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
-            mbar_expect_tx(full_bar(stage), STAGE_BYTES);  // own A + both halves of B
-            tma_load_3d(sa, ma, full_bar(stage), S.a_k0 + kb * BK, arow, ab);
+            if constexpr (TWO_SM) {
+              // both CTAs' copies complete CTA 0's barrier, which expects the pair's bytes
+              const uint32_t fb = mapa_rank0(full_bar(stage));
+              if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+              tma_load_3d_pair(sa, ma, fb, S.a_k0 + kb * BK, arow, ab);
 #pragma unroll
-            for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); ++j)  // this CTA's half of B
-              tma_load_3d_multicast(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb,
-                                    kPair);
+              for (int j = 0; j < BN / 128; ++j)  // this CTA's 128 columns of B
+                tma_load_3d_pair(sb + j * B_BOX_BYTES, mb, fb, bcol + rank * (BN / 2) + 64 * j, S.b_k0 + kb * BK,
+                                 bb);
+            } else {
+              mbar_expect_tx(full_bar(stage), STAGE_BYTES);  // own A + both halves of B
+              tma_load_3d(sa, ma, full_bar(stage), S.a_k0 + kb * BK, arow, ab);
+#pragma unroll
+              for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); ++j)  // this CTA's half of B
+                tma_load_3d_multicast(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb,
+                                      kPair);
+            }
             issued[stage] = true;
             issued_parity[stage] = phase;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
       }
-      if (!ok) {  // let copies already in flight land before the CTA exits
+      if (!ok && (!TWO_SM || rank == 0)) {  // let copies in flight land (pair: CTA 0's barriers count both)
         int dummy = 0;
         volatile int* never = &dummy;
         for (int s = 0; s < STAGES; ++s)
@@ -444,7 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (!TWO_SM || rank == 0)) {  // pair MMA: CTA 0 issues for both
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -468,18 +540,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 
             const uint32_t sb = sa + A_BYTES;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              umma(d, desc_a(sa + 32 * k), desc_b(sb + 2048 * k), P.idesc, accumulate);
+              if constexpr (TWO_SM) umma_pair(d, desc_a(sa + 32 * k), desc_b(sb + 2048 * k), P.idesc, accumulate);
+              else umma(d, desc_a(sa + 32 * k), desc_b(sb + 2048 * k), P.idesc, accumulate);
               accumulate = 1;
             }
             any_mma = true;
-            umma_commit_multicast(empty_bar(stage), kPair);  // both producers may refill this stage
+            // both producers may refill this stage
+            if constexpr (TWO_SM) umma_commit_pair(empty_bar(stage), kPair);
+            else umma_commit_multicast(empty_bar(stage), kPair);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
-        if (ok) umma_commit(tfull_bar(acc));
+        if (ok) {
+          if constexpr (TWO_SM) umma_commit_pair(tfull_bar(acc), kPair);  // both epilogues may read their halves
+          else umma_commit(tfull_bar(acc));
+        }
       }
       if (!ok && any_mma) {  // wait for the MMAs already issued before TMEM is freed
-        umma_commit(drain_bar);
+        if constexpr (TWO_SM) umma_commit_pair(drain_bar, 0x1);
+        else umma_commit(drain_bar);
         int dummy = 0;
         volatile int* never = &dummy;
         mbar_wait(drain_bar, 0, never);
@@ -593,7 +672,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 
         }
         if (last) {  // the accumulator is in registers: hand TMEM back to the MMA warp now
           tc_fence_before();
-          mbar_arrive(tempty_bar(acc));
+          __syncwarp();  // every lane's TMEM loads are complete before one lane releases for the warp
+          if (lane == 0) {
+            if constexpr (TWO_SM) mbar_arrive_cluster(mapa_rank0(tempty_bar(acc)));
+            else mbar_arrive(tempty_bar(acc));
+          }
         }
         // the strip about to be overwritten was handed to a bulk store two chunks ago
         if (lane == 0) bulk_wait_read_le1();
@@ -648,7 +731,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::THREADS, 
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc<TWO_SM>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -708,7 +791,7 @@ bool encode_out(CUtensorMap* map, const OutView& o, int dtype) {
   return r == CUDA_SUCCESS;
 }
 
-bool smem_configured[2][64] = {{false}};
+bool smem_configured[4][64] = {{false}};
 
 }  // namespace
 
@@ -726,14 +809,30 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
   if (!encode_fn()) return cudaErrorNotSupported;
   const bool far = plan.mode == EPI_FUSED_ALLREDUCE;
   if (far && plan.out_dtype == COCO_F32) return cudaErrorNotSupported;
-  auto kernel = far ? k_gemm_tc<EPI_FUSED_ALLREDUCE> : k_gemm_tc<EPI_STORE>;
+  // k-blocks per tile, averaged over the plan's jobs
+  int64_t kb_sum = 0;
+  for (const Job& J : plan.jobs)
+    for (int k = 0; k < J.nseg; ++k) kb_sum += (plan.segs[J.seg0 + k].klen + BK - 1) / BK;
+  const bool two_sm = plan.jobs.empty() ? true : kb_sum >= static_cast<int64_t>(kTwoSmMinKBlocks) * plan.jobs.size();
+  const int variant = (far ? 2 : 0) + (two_sm ? 1 : 0);
+  void (*kernel)(TcParams) = nullptr;
+  int smem = 0, threads = 0;
+  switch (variant) {
+    case 0: kernel = k_gemm_tc<EPI_STORE, false>; smem = Cfg<EPI_STORE, false>::SMEM_BYTES;
+            threads = Cfg<EPI_STORE, false>::THREADS; break;
+    case 1: kernel = k_gemm_tc<EPI_STORE, true>; smem = Cfg<EPI_STORE, true>::SMEM_BYTES;
+            threads = Cfg<EPI_STORE, true>::THREADS; break;
+    case 2: kernel = k_gemm_tc<EPI_FUSED_ALLREDUCE, false>; smem = Cfg<EPI_FUSED_ALLREDUCE, false>::SMEM_BYTES;
+            threads = Cfg<EPI_FUSED_ALLREDUCE, false>::THREADS; break;
+    default: kernel = k_gemm_tc<EPI_FUSED_ALLREDUCE, true>; smem = Cfg<EPI_FUSED_ALLREDUCE, true>::SMEM_BYTES;
+             threads = Cfg<EPI_FUSED_ALLREDUCE, true>::THREADS; break;
+  }
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !smem_configured[far][dev]) {
-    const int smem = far ? Cfg<EPI_FUSED_ALLREDUCE>::SMEM_BYTES : Cfg<EPI_STORE>::SMEM_BYTES;
+  if (dev >= 0 && dev < 64 && !smem_configured[variant][dev]) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    smem_configured[far][dev] = true;
+    smem_configured[variant][dev] = true;
   }
   // A-views are used with the A box and B-views with the B box; a view used
   // on both sides gets two maps.
@@ -741,8 +840,11 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
   cudaError_t status = cudaSuccess;
   size_t j = 0;
   const int fmt = plan.in_dtype == COCO_BF16 ? 1 : 0;
+  // instruction descriptor: f32 accumulator, A and B of the input type, A K-major, B N-major,
+  // N = 256, M = 128 per CTA (256 for the pair MMA)
+  const uint32_t mma_m = two_sm ? 2 * BM : BM;
   const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
-                         (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
+                         (static_cast<uint32_t>(BN >> 3) << 17) | ((mma_m >> 4) << 24);
   while (j < plan.jobs.size() && status == cudaSuccess) {
     memset(P, 0, sizeof(TcParams));
     std::vector<int> amap(plan.views.size(), -1), bmap(plan.views.size(), -1);
@@ -813,10 +915,7 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
     P->dropout = plan.far.dropout ? 1 : 0;
     const int pairs = sm_count() / 2;  // persistent: one CTA pair per two SMs
     const int grid = 2 * (tiles < pairs ? tiles : pairs);
-    if (far)
-      kernel<<<grid, Cfg<EPI_FUSED_ALLREDUCE>::THREADS, Cfg<EPI_FUSED_ALLREDUCE>::SMEM_BYTES, s>>>(*P);
-    else
-      kernel<<<grid, Cfg<EPI_STORE>::THREADS, Cfg<EPI_STORE>::SMEM_BYTES, s>>>(*P);
+    kernel<<<grid, threads, smem, s>>>(*P);
     count_launch();
     status = cudaGetLastError();
   }
