@@ -49,16 +49,22 @@ constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 
 // shared memory (tcgen05 cta_group::2), each CTA holding its own A tile and
 // its own 128-column half of B, 32 KB per stage, 6 stages. Four epilogue
 // warps (one per TMEM lane quarter) in both.
+//
+// The FusedAllReduce epilogue adds a third strip per epilogue warp, which the
+// residual tile is loaded into by TMA (one mbarrier per warp), and gives up
+// one or two stages for it.
 template <int MODE, bool TWO_SM>
 struct Cfg {
   static constexpr int B_STAGE = TWO_SM ? B_BYTES / 2 : B_BYTES;
   static constexpr int STAGE = A_BYTES + B_STAGE;
-  static constexpr int STAGES = TWO_SM ? 6 : 4;
+  static constexpr int STAGES = MODE == 0 ? (TWO_SM ? 6 : 4) : (TWO_SM ? 5 : 3);
   static constexpr int EPI_WARPS = 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int EPI_OFF = STAGES * STAGE;
-  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * 2 * EPI_STRIP;  // two strips per epilogue warp
-  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
+  static constexpr int STRIPS = MODE == 0 ? 2 : 3;  // two output strips (+ the residual strip)
+  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STRIPS * EPI_STRIP;
+  // full, empty, tmem full x2, tmem empty x2, drain (+ one residual barrier per epilogue warp)
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + (MODE == 0 ? 0 : EPI_WARPS);
   static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
 };
@@ -447,6 +453,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       mbar_init(tempty_bar(a), (TWO_SM ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (MODE == EPI_FUSED_ALLREDUCE)
+      for (int w = 0; w < EPI_WARPS; ++w) mbar_init(bar0 + 8u * (2 * STAGES + 5 + w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -567,7 +575,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
   } else {
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    const uint32_t strips = sbase + EPI_OFF + (warp - 2) * 2 * EPI_STRIP;
+    const uint32_t strips = sbase + EPI_OFF + (warp - 2) * C::STRIPS * EPI_STRIP;
+    const uint32_t res_strip = strips + 2 * EPI_STRIP;  // fused mode only
+    const uint32_t res_bar = bar0 + 8u * (2 * STAGES + 5 + (warp - 2));
+    uint32_t res_phase = 0;
+    bool res_pending = false;
     // with 8 epilogue warps, warps 2..5 take columns [0, BN/2) and warps 6..9 [BN/2, BN)
     constexpr int COLS = EPI_WARPS == 8 ? BN / 2 : BN;
     const int col_begin = EPI_WARPS == 8 ? ((warp - 2) >> 2) * COLS : 0;
@@ -604,22 +616,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       const bool bulk = (T.mt * BM + BM <= J.m || J.o_r0 + J.m == O.rows) &&
                         (T.nt * BN + BN <= J.n || J.o_c0 + J.n == O.cols);
       const int64_t obatch = static_cast<int64_t>(J.o_b0 + T.bb) * O.bstride;
-      // FusedAllReduce: this lane's residual row segment for the next chunk is
-      // requested one chunk ahead, so its latency overlaps the current chunk.
+      // FusedAllReduce: the residual's 32 x 64 strip of this warp is loaded by TMA one
+      // chunk ahead into the residual strip, and each lane reads its row from there.
       const int jrow = row0 + lane;
       const int64_t grow = J.o_r0 + jrow;
-      uint4 rv[8];
-      auto load_residual = [&](int cc) {
-        const int gc = J.o_c0 + T.nt * BN + cc;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          rv[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (J.res && jrow < J.m && gc + i * 8 < O.cols && cc < col_begin + COLS)
-            rv[i] = ld_nc_v4_hint(static_cast<const char*>(J.res) + (obatch + grow * O.ld + gc + i * 8) * 2,
-                                  evict_first);
-        }
+      const bool has_res = MODE == EPI_FUSED_ALLREDUCE && J.res != nullptr;
+      auto load_residual = [&](int cc) {  // lane 0 only
+        mbar_expect_tx(res_bar, EPI_STRIP);
+        tma_load_3d(res_strip, &P.omaps[J.res_map], res_bar, J.o_c0 + T.nt * BN + cc, J.o_r0 + row0,
+                    J.o_b0 + T.bb);
       };
-      if constexpr (MODE == EPI_FUSED_ALLREDUCE) load_residual(col_begin);
+      if (has_res && lane == 0) {
+        load_residual(col_begin);
+        res_pending = true;
+      }
       for (int c0 = col_begin; c0 < col_begin + COLS; c0 += cols_per_chunk) {
         const bool last = c0 + cols_per_chunk >= col_begin + COLS;
         uint32_t p[32];
@@ -627,9 +637,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
           // 16-bit output: 64 columns of this lane's row
           const int gcol0 = J.o_c0 + T.nt * BN + c0;
           uint4 cur[8];
+          if (has_res) {
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(res_bar, res_phase, abort_flag));
+            if (!landed) {
+              if (lane == 0) fail();
+              break;
+            }
+            res_phase ^= 1u;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) cur[i] = rv[i];
-          if (!last) load_residual(c0 + cols_per_chunk);
+            for (int c = 0; c < 8; ++c) cur[c] = ld_shared_v4(res_strip + lane * 128 + ((c ^ (lane & 7)) << 4));
+            fence_proxy_async_smem();  // these reads come before the next TMA write of the strip
+            __syncwarp();
+            if (lane == 0) {
+              res_pending = !last;
+              if (!last) load_residual(c0 + cols_per_chunk);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) cur[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
           uint32_t r[32], r2[32];
           tmem_ld32(tbase + c0, r);
           tmem_ld32(tbase + c0 + 32, r2);
@@ -721,7 +747,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
         buf ^= 1;
       }
     }
-    if (lane == 0) bulk_wait_all();  // bulk stores finish before the CTA's shared memory goes away
+    if (lane == 0) {
+      if (res_pending) {  // an aborted tile may leave a residual load in flight
+        int dummy = 0;
+        volatile int* never = &dummy;
+        mbar_wait(res_bar, res_phase, never);
+      }
+      bulk_wait_all();  // bulk stores finish before the CTA's shared memory goes away
+    }
     __syncwarp();
   }
 
@@ -863,7 +896,7 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
       int found = -1;
       for (size_t q = 0; q < orange.size(); ++q)
         if (orange[q].first == J.out && orange[q].second == J.nout) found = obase[q];
-      const int need_out = found < 0 ? J.nout : 0;
+      const int need_out = (found < 0 ? J.nout : 0) + (far && J.res ? 1 : 0);
       if (nmaps + need_maps > MAX_MAPS || nsegs + J.nseg > MAX_SEGS || nouts + need_out > MAX_OUTS) break;
       Job nj = J;
       nj.seg0 = static_cast<int16_t>(nsegs);
@@ -894,6 +927,13 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
         obase.push_back(found);
       }
       nj.out = found;
+      nj.res_map = -1;
+      if (far && J.res) {  // the residual has the output's shape: a map like the outputs' (box 32 rows)
+        OutView rv = plan.outs[J.out];
+        rv.ptr = const_cast<void*>(J.res);
+        if (!encode_out(&P->omaps[nouts], rv, plan.out_dtype)) { status = cudaErrorInvalidValue; break; }
+        nj.res_map = static_cast<int16_t>(nouts++);
+      }
       P->jobs[njobs] = nj;
       P->unit_start[njobs] = tiles;
       tiles += J.nb * ((J.m + 2 * BM - 1) / (2 * BM)) * ((J.n + BN - 1) / BN);

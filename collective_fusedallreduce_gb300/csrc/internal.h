@@ -99,7 +99,8 @@ struct Job {
   int32_t o_b0, o_r0, o_c0;
   int32_t nb, m, n;
   int16_t seg0, nseg;
-  int16_t nout, pad_;
+  int16_t nout;
+  int16_t res_map;  // FusedAllReduce epilogue: index of the residual's tensor map in the launch (set there)
   const void* res;
 };
 
