@@ -9,17 +9,22 @@
 // order of K-segments (Addition: accumulated in TMEM) or of output jobs
 // (DynamicUpdateSlice: the epilogue's row / column / batch offset).
 //
-// Kernel shape (one CTA per SM, persistent over tiles):
-//   warp 0      TMA producer: A tile [128 x 64] (K-major, 128B swizzle) and
-//               B tile [64 x 256] (N-major: four 64-column boxes, 128B
-//               swizzle) per stage, into a 4-stage mbarrier ring.
-//   warp 1      allocates 512 TMEM columns (two fp32 128x256 accumulators),
-//               one thread issues tcgen05.mma (M=128, N=256, K=16) and
-//               commits stages back to the producer and finished
-//               accumulators to the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, convert, stage a
-//               128-byte-wide swizzled strip in shared memory, then coalesced
-//               16-byte global stores bounded by the job's extent.
+// Kernel shape (one CTA per SM, CTA pairs in clusters of two, persistent
+// over work units of two vertically adjacent 128 x 256 output tiles):
+//   warp 0      TMA producer: per k-block (64 deep) an A tile [128 x 64]
+//               (K-major, 128B swizzle) and B columns (N-major, 64-column
+//               boxes, 128B swizzle) into an mbarrier ring of stages.
+//   warp 1      allocates 512 TMEM columns (two fp32 128 x 256 accumulators)
+//               and issues tcgen05.mma from one elected lane: either one
+//               M=128, N=256 MMA per CTA, the pair sharing B by TMA multicast
+//               (4 stages of 48 KB), or, for long k-loops, one M=256 MMA over
+//               both CTAs (tcgen05 cta_group::2, 6 stages of 32 KB per CTA).
+//   warps 2..5  epilogue, one TMEM lane quarter each: tcgen05.ld 32 lanes x
+//               32 columns, convert (or, for the FusedAllReduce, add bias,
+//               apply dropout and add the residual), stage a 128-byte-wide
+//               swizzled strip in shared memory and bulk-store it by TMA;
+//               tiles that overhang their job's region use bounded 16-byte
+//               stores instead.
 // Every mbarrier wait is bounded by %globaltimer; on expiry the kernel records
 // COCO_ERR_TIMEOUT in the error word, raises an abort flag for the other
 // roles, drains its own outstanding copies / MMAs (bounded again), frees TMEM
@@ -134,8 +139,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait. Returns false on timeout or when another role aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_test(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
@@ -144,6 +148,29 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       if (globaltimer() - t0 > kTimeoutNs) return false;
     }
   }
+}
+// The common case (phase already complete) stays inline.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  return mbar_test(bar, parity) || mbar_wait_slow(bar, parity, abort_flag);
+}
+// The same for a whole warp, with one answer for all its lanes. Only lane 0
+// polls a phase that is not complete yet; the lanes that issue async
+// operations afterwards are lane 0 (the elected lane of a converged warp).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_slow(bar, parity, abort_flag);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+// One lane of a converged warp (the lowest), chosen by the hardware.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(p));
+  return p != 0;
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
@@ -201,6 +228,18 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+// Accumulator hand-back arrivals (own CTA / CTA 0 of the pair) with relaxed
+// semantics. Nothing in memory is published by them: the TMEM loads they
+// announce have completed (tcgen05.wait::ld) and are ordered before the
+// arrival by tcgen05.fence::before_thread_sync. A release arrival would also
+// wait for this thread's earlier writes to become visible, which costs over a
+// thousand cycles per tile at cluster scope.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -469,14 +508,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
     atomicCAS(P.err, 0u, static_cast<unsigned int>(COCO_ERR_TIMEOUT));
   };
 
+  // The MMA role is run by a whole warp so that every loop value is
+  // warp-uniform; one elected lane issues the MMAs. Run by a single lane, the
+  // same loop keeps its values in per-thread registers and no longer keeps the
+  // tensor pipe fed. The producer is run the same way for the pair MMA, whose
+  // long, operand-bound k-loops gain from it (the K=512 MatMul: 10 % faster);
+  // with one CTA per MMA (short k-loops whose tiles are store-bound, like the
+  // K=128 batched einsum) a single-lane producer measured 10 % faster.
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // (lanes 1..31 of a single-lane producer go straight to the final barrier)
+    if (TWO_SM || lane == 0) {
+      const bool leader = TWO_SM ? elect_one() : true;
+      auto wait = [&](uint32_t bar, uint32_t parity, volatile int* flag) {
+        if constexpr (TWO_SM) return mbar_wait_warp(bar, parity, flag);
+        else return mbar_wait(bar, parity, flag);
+      };
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_parity[STAGES];
-      bool issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) { issued[s] = false; issued_parity[s] = 0; }
+      uint32_t issued = 0, issued_parity = 0;  // per stage: a copy was issued, and the phase it completes
       bool ok = true;
       for (int u = cluster_id; ok && u < P.total_units; u += nclusters) {
         const Tile T = decode_unit(P, u, rank);
@@ -489,28 +539,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
           const int arow = S.a_r0 + T.mt * BM, ab = S.a_b0 + T.bb;
           const int bcol = S.b_c0 + T.nt * BN, bb = S.b_b0 + T.bb;
           for (int kb = 0; kb < kblocks; ++kb) {
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) { fail(); ok = false; break; }
+            if (!wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+              if (leader) fail();
+              ok = false;
+              break;
+            }
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
-            if constexpr (TWO_SM) {
-              // both CTAs' copies complete CTA 0's barrier, which expects the pair's bytes
-              const uint32_t fb = mapa_rank0(full_bar(stage));
-              if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
-              tma_load_3d_pair(sa, ma, fb, S.a_k0 + kb * BK, arow, ab);
+            if (leader) {
+              if constexpr (TWO_SM) {
+                // both CTAs' copies complete CTA 0's barrier, which expects the pair's bytes
+                const uint32_t fb = mapa_rank0(full_bar(stage));
+                if (rank == 0) mbar_expect_tx(full_bar(stage), 2 * STAGE_BYTES);
+                tma_load_3d_pair(sa, ma, fb, S.a_k0 + kb * BK, arow, ab);
 #pragma unroll
-              for (int j = 0; j < BN / 128; ++j)  // this CTA's 128 columns of B
-                tma_load_3d_pair(sb + j * B_BOX_BYTES, mb, fb, bcol + rank * (BN / 2) + 64 * j, S.b_k0 + kb * BK,
-                                 bb);
-            } else {
-              mbar_expect_tx(full_bar(stage), STAGE_BYTES);  // own A + both halves of B
-              tma_load_3d(sa, ma, full_bar(stage), S.a_k0 + kb * BK, arow, ab);
+                for (int j = 0; j < BN / 128; ++j)  // this CTA's 128 columns of B
+                  tma_load_3d_pair(sb + j * B_BOX_BYTES, mb, fb, bcol + rank * (BN / 2) + 64 * j, S.b_k0 + kb * BK,
+                                   bb);
+              } else {
+                mbar_expect_tx(full_bar(stage), STAGE_BYTES);  // own A + both halves of B
+                tma_load_3d(sa, ma, full_bar(stage), S.a_k0 + kb * BK, arow, ab);
 #pragma unroll
-              for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); ++j)  // this CTA's half of B
-                tma_load_3d_multicast(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb,
-                                      kPair);
+                for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); ++j)  // this CTA's half of B
+                  tma_load_3d_multicast(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb,
+                                        kPair);
+              }
             }
-            issued[stage] = true;
-            issued_parity[stage] = phase;
+            if constexpr (TWO_SM) __syncwarp();
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
@@ -519,57 +576,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
         int dummy = 0;
         volatile int* never = &dummy;
         for (int s = 0; s < STAGES; ++s)
-          if (issued[s]) mbar_wait(full_bar(s), issued_parity[s], never);
+          if ((issued >> s) & 1u) wait(full_bar(s), (issued_parity >> s) & 1u, never);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0 && (!TWO_SM || rank == 0)) {  // pair MMA: CTA 0 issues for both
+    if (!TWO_SM || rank == 0) {  // pair MMA: CTA 0 issues for both
+      // The tensor pipe finishes a k-block (four K=16 MMAs) in about 512
+      // cycles, so per-k-block work stays at a few instructions: descriptors
+      // advance by adding to the encoded start address (stage offsets stay
+      // below the 14-bit field's limit, as shared memory ends below 256 KB),
+      // the job is followed by a forward scan (units increase monotonically),
+      // and only the k-block count is read per tile. tcgen05.commit tracks the
+      // MMAs of the thread that issues it, so one lane issues both.
+      const bool leader = elect_one();
+      const uint32_t idesc = P.idesc;
+      const uint64_t adesc0 = desc_a(sbase), bdesc0 = desc_b(sbase + A_BYTES);
+      constexpr uint32_t kStageDesc = static_cast<uint32_t>(STAGE_BYTES >> 4);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
+      int job = 0;
       bool ok = true;
       bool any_mma = false;
       for (int u = cluster_id; ok && u < P.total_units; u += nclusters, ++local) {
-        const Tile T = decode_unit(P, u, rank);
-        const Job J = P.jobs[T.job];  // a register copy: asm memory clobbers would force reloads
+        while (job + 1 < P.njobs && P.unit_start[job + 1] <= u) ++job;
+        const int kblocks = P.jobs[job].kblocks;
         const int acc = local & 1;
         const uint32_t aph = (local >> 1) & 1;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) { fail(); ok = false; break; }
+        if (!mbar_wait_warp(tempty_bar(acc), aph ^ 1u, abort_flag)) {
+          if (leader) fail();
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        uint32_t accumulate = 0;
-        for (int si = 0; ok && si < J.nseg; ++si) {
-          const int kblocks = (static_cast<int>(P.segs[J.seg0 + si].klen) + BK - 1) / BK;
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!mbar_wait(full_bar(stage), phase, abort_flag)) { fail(); ok = false; break; }
-            tc_fence_after();
-            const uint32_t sa = sbase + stage * STAGE_BYTES;
-            const uint32_t sb = sa + A_BYTES;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait_warp(full_bar(stage), phase, abort_flag)) {
+            if (leader) fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t off = static_cast<uint64_t>(stage * kStageDesc);
+          const uint64_t ad = adesc0 + off, bd = bdesc0 + off;
+          if (leader) {
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              if constexpr (TWO_SM) umma_pair(d, desc_a(sa + 32 * k), desc_b(sb + 2048 * k), P.idesc, accumulate);
-              else umma(d, desc_a(sa + 32 * k), desc_b(sb + 2048 * k), P.idesc, accumulate);
-              accumulate = 1;
+              // K-major A: the k-th K=16 slice is 32 B further; N-major B: 2048 B (in 16-byte units)
+              const uint32_t accumulate = (kb | k) != 0;
+              if constexpr (TWO_SM) umma_pair(d, ad + 2 * k, bd + 128 * k, idesc, accumulate);
+              else umma(d, ad + 2 * k, bd + 128 * k, idesc, accumulate);
             }
-            any_mma = true;
             // both producers may refill this stage
             if constexpr (TWO_SM) umma_commit_pair(empty_bar(stage), kPair);
             else umma_commit_multicast(empty_bar(stage), kPair);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
+          __syncwarp();
+          any_mma = true;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (ok) {
+        if (ok && leader) {
           if constexpr (TWO_SM) umma_commit_pair(tfull_bar(acc), kPair);  // both epilogues may read their halves
           else umma_commit(tfull_bar(acc));
         }
+        __syncwarp();
       }
       if (!ok && any_mma) {  // wait for the MMAs already issued before TMEM is freed
-        if constexpr (TWO_SM) umma_commit_pair(drain_bar, 0x1);
-        else umma_commit(drain_bar);
+        if (leader) {
+          if constexpr (TWO_SM) umma_commit_pair(drain_bar, 0x1);
+          else umma_commit(drain_bar);
+        }
+        __syncwarp();
         int dummy = 0;
         volatile int* never = &dummy;
-        mbar_wait(drain_bar, 0, never);
+        mbar_wait_warp(drain_bar, 0, never);
       }
     }
   } else {
@@ -700,8 +781,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
           tc_fence_before();
           __syncwarp();  // every lane's TMEM loads are complete before one lane releases for the warp
           if (lane == 0) {
-            if constexpr (TWO_SM) mbar_arrive_cluster(mapa_rank0(tempty_bar(acc)));
-            else mbar_arrive(tempty_bar(acc));
+            if constexpr (TWO_SM) mbar_arrive_cluster_relaxed(mapa_rank0(tempty_bar(acc)));
+            else mbar_arrive_relaxed(tempty_bar(acc));
           }
         }
         // the strip about to be overwritten was handed to a bulk store two chunks ago
@@ -934,6 +1015,9 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
         if (!encode_out(&P->omaps[nouts], rv, plan.out_dtype)) { status = cudaErrorInvalidValue; break; }
         nj.res_map = static_cast<int16_t>(nouts++);
       }
+      nj.kblocks = 0;
+      for (int k = 0; k < J.nseg; ++k) nj.kblocks += (plan.segs[J.seg0 + k].klen + BK - 1) / BK;
+      if (nj.kblocks <= 0) { status = cudaErrorInvalidValue; break; }  // an empty contraction is zero-filled, not run
       P->jobs[njobs] = nj;
       P->unit_start[njobs] = tiles;
       tiles += J.nb * ((J.m + 2 * BM - 1) / (2 * BM)) * ((J.n + BN - 1) / BN);

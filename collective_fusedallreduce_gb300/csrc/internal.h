@@ -101,6 +101,7 @@ struct Job {
   int16_t seg0, nseg;
   int16_t nout;
   int16_t res_map;  // FusedAllReduce epilogue: index of the residual's tensor map in the launch (set there)
+  int32_t kblocks;  // K blocks of the tile's whole segment loop (set by the tensor-core launcher)
   const void* res;
 };
 
