@@ -683,14 +683,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       const OutView O = P.outs[J.out];
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
-      // all lanes must agree before the warp-collective TMEM loads
-      const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag));
-      if (!ready) {
-        if (lane == 0) fail();
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       const int row0 = T.mt * BM + quarter * 32;  // job-relative row of this warp's lane 0
       // A bulk store clips only at the tensor's edges, so it is used when the
       // tile lies inside its job's region or overhangs only past the tensor.
@@ -707,10 +699,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
         tma_load_3d(res_strip, &P.omaps[J.res_map], res_bar, J.o_c0 + T.nt * BN + cc, J.o_r0 + row0,
                     J.o_b0 + T.bb);
       };
-      if (has_res && lane == 0) {
-        load_residual(col_begin);
-        res_pending = true;
+      // Operands of the FusedAllReduce epilogue that do not depend on the
+      // accumulator are requested before it is ready: the first residual strip
+      // (the strip is free: the previous tile's last chunk issued no load), and
+      // the bias, lane l holding tile columns [8l, 8l + 8) for the lanes that
+      // need them (shuffles), instead of one dependent global load per column group.
+      uint4 bias_v = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (MODE == EPI_FUSED_ALLREDUCE) {
+        if (has_res && lane == 0) {
+          load_residual(col_begin);
+          res_pending = true;
+        }
+        const int bc = J.o_c0 + T.nt * BN + 8 * lane;
+        if (bias_ptr && bc < O.cols) bias_v = ld_nc_v4(bias_ptr + bc * 2);
       }
+      // all lanes must agree before the warp-collective TMEM loads
+      const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag));
+      if (!ready) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       for (int c0 = col_begin; c0 < col_begin + COLS; c0 += cols_per_chunk) {
         const bool last = c0 + cols_per_chunk >= col_begin + COLS;
         uint32_t p[32];
@@ -745,12 +755,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float bias[8], res[8], v[8];
-            if (bias_ptr && gcol0 + i * 8 < O.cols) {  // the same address in every lane: one broadcast load
-              unpack8(ld_nc_v4(bias_ptr + (gcol0 + i * 8) * 2), out_dt, bias);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) bias[j] = 0.0f;
-            }
+            const int src = (c0 >> 3) + i;  // the lane holding tile columns c0 + 8i .. + 7
+            uint4 bv;
+            bv.x = __shfl_sync(0xffffffffu, bias_v.x, src);
+            bv.y = __shfl_sync(0xffffffffu, bias_v.y, src);
+            bv.z = __shfl_sync(0xffffffffu, bias_v.z, src);
+            bv.w = __shfl_sync(0xffffffffu, bias_v.w, src);
+            unpack8(bv, out_dt, bias);
             unpack8(cur[i], out_dt, res);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
