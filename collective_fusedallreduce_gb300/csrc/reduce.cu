@@ -23,7 +23,7 @@ namespace coco {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 2;
+constexpr int kUnroll = 1;
 
 // ---------------------------------------------------------------- vectors
 
@@ -124,9 +124,12 @@ struct FarArgs {
   uint64_t seed;
 };
 
-// NR: compile-time rank count (0 = runtime, processed 8 at a time).
+// NR: compile-time rank count (0 = runtime, processed 8 at a time). Every
+// stream of a vector (the ranks' partials, the residual, the bias) is requested
+// before any is used, so a warp waits for memory once per vector; three
+// blocks per SM (at most 85 registers a thread) keep enough of these in flight.
 template <typename T, int NR, bool DROP>
-__global__ void __launch_bounds__(kThreads) k_fused_allreduce(const __grid_constant__ FarArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) k_fused_allreduce(const __grid_constant__ FarArgs a) {
   using V = V16<T>;
   constexpr int VE = V::N;
   const int g = blockIdx.y;
@@ -145,13 +148,22 @@ __global__ void __launch_bounds__(kThreads) k_fused_allreduce(const __grid_const
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) vi[u] = base + u * kThreads;
 
+    uint4 resv[kUnroll], biasv[kUnroll];
     if constexpr (NR > 0) {
       uint4 raw[kUnroll][NR];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
+      for (int u = 0; u < kUnroll; ++u) {
 #pragma unroll
         for (int r = 0; r < NR; ++r)
           if (vi[u] < a.nvec) raw[u][r] = ld_stream(static_cast<const char*>(in[r]) + vi[u] * 16);
+        if (vi[u] < a.nvec && res) resv[u] = ld_stream(res + vi[u] * 16);
+        if (vi[u] < a.nvec && bias) {
+          const int64_t bv = a.nvec < (int64_t(1) << 31)
+                                 ? static_cast<int64_t>(static_cast<uint32_t>(vi[u]) % static_cast<uint32_t>(a.bias_vecs))
+                                 : vi[u] % a.bias_vecs;
+          biasv[u] = *reinterpret_cast<const uint4*>(bias + bv * 16);
+        }
+      }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         if (vi[u] >= a.nvec) continue;
@@ -193,10 +205,14 @@ __global__ void __launch_bounds__(kThreads) k_fused_allreduce(const __grid_const
       if (v >= a.nvec) continue;
       if (bias) {
         float f[VE];
-        const int64_t bv = a.nvec < (int64_t(1) << 31)
-                               ? static_cast<int64_t>(static_cast<uint32_t>(v) % static_cast<uint32_t>(a.bias_vecs))
-                               : v % a.bias_vecs;
-        V::load(*reinterpret_cast<const uint4*>(bias + bv * 16), f);
+        if constexpr (NR > 0) {
+          V::load(biasv[u], f);
+        } else {
+          const int64_t bv = a.nvec < (int64_t(1) << 31)
+                                 ? static_cast<int64_t>(static_cast<uint32_t>(v) % static_cast<uint32_t>(a.bias_vecs))
+                                 : v % a.bias_vecs;
+          V::load(*reinterpret_cast<const uint4*>(bias + bv * 16), f);
+        }
 #pragma unroll
         for (int j = 0; j < VE; ++j) acc[u][j] += f[j];
       }
@@ -211,7 +227,8 @@ __global__ void __launch_bounds__(kThreads) k_fused_allreduce(const __grid_const
       }
       if (res) {
         float f[VE];
-        V::load(ld_stream(res + v * 16), f);
+        if constexpr (NR > 0) V::load(resv[u], f);
+        else V::load(ld_stream(res + v * 16), f);
 #pragma unroll
         for (int j = 0; j < VE; ++j) acc[u][j] += f[j];
       }

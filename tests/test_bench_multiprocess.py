@@ -62,6 +62,21 @@ def test_single_process_helpers_without_a_process_group():
     assert abs(bench.aggregate_value(1.0, 2.0, 1) - 50.0) < 1e-12
 
 
+def test_roofline_peak_follows_the_power_regime():
+    """Tensor-bound kernels are held to the burst bf16 figure, or to the sustained one when the
+    clock record saw sw_power_cap; HBM-bound kernels always to the copy figure."""
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "source": "measured"}
+    burst = bench.roofline_entry("k", "tensor", 1.6e12, 1e-3, peaks, None, False)
+    assert burst["peak"] == 2000.0 and abs(burst["frac"] - 0.8) < 1e-9 and "frac_of_burst" not in burst
+    capped = bench.roofline_entry("k", "tensor", 1.6e12, 1e-3, peaks, 123, True)
+    assert capped["peak"] == 1600.0 and abs(capped["frac"] - 1.0) < 1e-9
+    assert abs(capped["frac_of_burst"] - 0.8) < 1e-9 and capped["traffic"] == 123
+    hbm = bench.roofline_entry("k", "hbm", 3e9, 1e-3, peaks, None, True)
+    assert hbm["peak"] == 6000.0 and abs(hbm["frac"] - 0.5) < 1e-9
+
+
 def test_reference_arm_under_torchrun_two_ranks():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
