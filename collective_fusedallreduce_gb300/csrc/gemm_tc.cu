@@ -684,15 +684,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       const int row0 = T.mt * BM + quarter * 32;  // job-relative row of this warp's lane 0
-      // A bulk store clips only at the tensor's edges, so it is used when the
-      // tile lies inside its job's region or overhangs only past the tensor.
-      const bool bulk = (T.mt * BM + BM <= J.m || J.o_r0 + J.m == O.rows) &&
-                        (T.nt * BN + BN <= J.n || J.o_c0 + J.n == O.cols);
-      const int64_t obatch = static_cast<int64_t>(J.o_b0 + T.bb) * O.bstride;
-      // FusedAllReduce: the residual's 32 x 64 strip of this warp is loaded by TMA one
-      // chunk ahead into the residual strip, and each lane reads its row from there.
-      const int jrow = row0 + lane;
-      const int64_t grow = J.o_r0 + jrow;
       const bool has_res = MODE == EPI_FUSED_ALLREDUCE && J.res != nullptr;
       auto load_residual = [&](int cc) {  // lane 0 only
         mbar_expect_tx(res_bar, EPI_STRIP);
@@ -721,6 +712,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      // A bulk store clips only at the tensor's edges, so it is used when the
+      // tile lies inside its job's region or overhangs only past the tensor.
+      const bool bulk = (T.mt * BM + BM <= J.m || J.o_r0 + J.m == O.rows) &&
+                        (T.nt * BN + BN <= J.n || J.o_c0 + J.n == O.cols);
+      const int64_t obatch = static_cast<int64_t>(J.o_b0 + T.bb) * O.bstride;
+      const int jrow = row0 + lane;
+      const int64_t grow = J.o_r0 + jrow;
       for (int c0 = col_begin; c0 < col_begin + COLS; c0 += cols_per_chunk) {
         const bool last = c0 + cols_per_chunk >= col_begin + COLS;
         uint32_t p[32];
