@@ -155,6 +155,10 @@ class Workload:
         """[(device tensor, pinned host copy)] re-uploaded every e2e step, and the result tensor read back."""
         raise NotImplementedError
 
+    def rebind(self, key):
+        """Called after the input tensors were pointed at buffer set ``key``: rebuild any state that holds
+        their addresses (none by default: every call reads the tensors' current pointers)."""
+
     def oracle_sample(self, rows):
         """Runs the oracle on a sample; returns the sample's fraction of the step's work."""
         raise NotImplementedError
@@ -578,6 +582,16 @@ class ScatteredGradients(Workload):
         if marks:
             marks[1].record(stream)
 
+    def rebind(self, key):
+        # the bucket table holds the tensors' addresses: one table per buffer set
+        from collective_fusedallreduce_gb300 import coco
+        if not hasattr(self, "_plans"):
+            self._plans = {0: (self.table, self.plan)}
+        if key not in self._plans:
+            table = torch.empty_like(self.table)
+            self._plans[key] = (table, coco.coco_scattered_table_build(self.grads, table))
+        self.table, self.plan = self._plans[key]
+
     def host_inputs(self):
         return [(t, t.cpu().pin_memory()) for row in self.grads for t in row], self.grads[0][0]
 
@@ -694,6 +708,88 @@ def max_over_ranks(x, dist, device):
 def aggregate_value(ideal_s, step_s, world):
     """Whole-job throughput: every replica processes one step's work per ``step_s``."""
     return 100.0 * ideal_s / step_s * world
+
+
+def measure_e2e(wl, stream, dev, dist, ideal, world, steps):
+    """The step end to end through the public calls: every step uploads its inputs from pinned host
+    memory and reads its result back, overlapping the compute of other steps; inputs and the result
+    are double-buffered, as a data loader would feed the step. The timed region spans the first
+    upload to the last read-back. Two arrangements are timed and the faster reported: uploads and
+    read-backs on one copy stream, or on two (concurrent directions); on GB300 the second wins for
+    small transfers and loses for multi-GB uploads, whose rate drops when read-backs run beside them."""
+    ins, result = wl.host_inputs()
+    devs = [d for d, _ in ins]
+    hosts = [h for _, h in ins]
+    in_place = any(d is result for d in devs)
+    sets = [[d.data for d in devs], [torch.empty_like(d) for d in devs]]
+    outs = [result.data, None if in_place else torch.empty_like(result)]
+    host_out = torch.empty(result.shape, dtype=result.dtype, pin_memory=True)
+    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    d2h = host_out.numel() * host_out.element_size()
+    up = torch.cuda.Stream(device=dev)
+    down = up
+    uploaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    downloaded = [torch.cuda.Event() for _ in range(2)]
+
+    def bind(b):
+        for d, storage in zip(devs, sets[b]):
+            d.data = storage
+        if not in_place:
+            result.data = outs[b]
+        wl.rebind(b)
+
+    def upload(b, after_step):
+        with torch.cuda.stream(up):
+            if after_step:  # set b is free once its last step has computed (and, in place, been read back)
+                up.wait_event(downloaded[b] if in_place else computed[b])
+            for storage, h in zip(sets[b], hosts):
+                storage.copy_(h, non_blocking=True)
+            uploaded[b].record(up)
+
+    def run(n):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0.record(up)
+        down.wait_event(e0)
+        stream.wait_event(e0)
+        upload(0, False)
+        if n > 1:
+            upload(1, False)
+        for k in range(n):
+            b = k % 2
+            stream.wait_event(uploaded[b])
+            if k >= 2:  # the result buffer of step k-2 has been read back
+                stream.wait_event(downloaded[b])
+            bind(b)
+            wl.step(stream)
+            computed[b].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[b])
+                host_out.copy_(result.data if in_place else outs[b], non_blocking=True)
+                downloaded[b].record(down)
+            if k + 2 < n:
+                upload(b, True)
+        e1.record(down)
+        torch.cuda.synchronize()
+        bind(0)
+        return e0.elapsed_time(e1) / 1000.0
+
+    best = None
+    for mode in ("one copy stream", "two copy streams"):
+        down = up if mode == "one copy stream" else torch.cuda.Stream(device=dev)
+        run(2)
+        et = max_over_ranks(run(steps), dist, dev)
+        if best is None or et < best[0]:
+            best = (et, mode)
+    et, mode = best
+    return {"value": aggregate_value(ideal, et / steps, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": 1000.0 * et / steps,
+            "overlap": f"uploads and read-backs overlap the compute of other steps ({mode}); inputs and result "
+                       "double-buffered"}
 
 
 # ------------------------------------------------------------------- main
@@ -827,31 +923,7 @@ def main():
 
     # end to end: host buffers in, result back, through the same public calls
     if not args.no_e2e:
-        ins, result = wl.host_inputs()
-        host_out = torch.empty(result.shape, dtype=result.dtype, pin_memory=True)
-        h2d = sum(h.numel() * h.element_size() for _, h in ins)
-        d2h = host_out.numel() * host_out.element_size()
-        ek = max(3, min(args.steps, 50))
-        for _ in range(2):
-            for d, h in ins:
-                d.copy_(h, non_blocking=True)
-            wl.step(stream)
-            host_out.copy_(result, non_blocking=True)
-        torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(ek):
-            for d, h in ins:
-                d.copy_(h, non_blocking=True)
-            wl.step(stream)
-            host_out.copy_(result, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        et = max_over_ranks(e0.elapsed_time(e1) / 1000.0, dist, dev)
-        line["e2e"] = {"value": aggregate_value(ideal, et / ek, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                       "d2h_bytes_per_step": d2h, "steps": ek, "ms_per_step": 1000.0 * et / ek}
+        line["e2e"] = measure_e2e(wl, stream, dev, dist, ideal, world, max(3, min(args.steps, 50)))
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, rows, frac = cpu_oracle_rate(wl, peaks, args.cpu_seconds)
