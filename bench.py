@@ -239,6 +239,50 @@ class MegatronTail(Workload):
         return self.rows
 
 
+class MegatronTailOverlap(MegatronTail):
+    """[CoCoNet] §5.3 Overlap: the same Fig. 3 tail with the rows cut into chunks; the FusedAllReduce of
+    chunk c (a second stream) runs while the MatMul computes chunk c+1. Stream order only: every
+    FusedAllReduce waits for its chunk's MatMul through an event, nothing spins on the device.
+    Dropout indices continue across chunks (coco_fused_allreduce_at), so the outputs equal the
+    unchunked step's bit for bit. Rated against the whole step's own roofline, max(MatMul FLOPs at
+    the tensor peak, MatMul + FusedAllReduce bytes at the HBM peak)."""
+
+    name = "megatron_attention_tail_overlap"
+
+    def __init__(self, dev, chunks=4, **kw):
+        super().__init__(dev, **kw)
+        self.chunks = chunks
+        self.side = torch.cuda.Stream(device=dev)
+        self.config = dict(self.config)
+        self.config["workload"] = self.config["workload"].replace(
+            "local MatMul -> FusedAllReduce",
+            f"local MatMul overlapped with FusedAllReduce in {chunks} row chunks (two streams)")
+        self.config["chunks"] = chunks
+
+    def gemm_bytes(self):
+        n, rows, h, ks = self.n, self.rows, self.h, self.ks
+        return (n * rows * ks + n * ks * h + n * rows * h) * 2
+
+    def timed(self):
+        flops = self.kernels()[0][2]
+        byts = self.kernels()[1][2] + self.gemm_bytes()
+        return [(f"MatMul || FusedAllReduce in {self.chunks} chunks (step bytes)", "hbm", byts, 1)]
+
+    def ideal_seconds(self, peaks):
+        flops = self.kernels()[0][2]
+        byts = self.kernels()[1][2] + self.gemm_bytes()
+        return max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+
+    def step(self, stream, marks=None):
+        from collective_fusedallreduce_gb300 import workloads
+        if marks:
+            marks[0].record(stream)
+        workloads.megatron_attention_tail_overlap(self.inp, self.w, self.bias, self.res, self.p, self.seed,
+                                                  self.chunks, self.layer, self.out, stream, self.side)
+        if marks:
+            marks[1].record(stream)
+
+
 class MegatronTailFused(MegatronTail):
     """The same Fig. 3 tail with the MatMul fused into the FusedAllReduce: one
     tensor-core kernel sums the 8 ranks' K-slices in TMEM and applies bias,
@@ -614,7 +658,7 @@ class ScatteredGradients(Workload):
         return self.numel // 4096
 
 
-WORKLOADS = {"c2": MegatronTail, "c2f": MegatronTailFused, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
+WORKLOADS = {"c2": MegatronTail, "c2o": MegatronTailOverlap, "c2f": MegatronTailFused, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
              "c5b": RsAg, "scatter": ScatteredGradients}
 
 

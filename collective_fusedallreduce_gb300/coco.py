@@ -71,6 +71,7 @@ _P = ctypes.POINTER(CocoTensor)
 _S = ctypes.c_void_p
 for _name, _args in {
     "coco_fused_allreduce": [_P, ctypes.c_void_p, _P, ctypes.c_float, ctypes.c_uint64, _P, _S],
+    "coco_fused_allreduce_at": [_P, ctypes.c_void_p, _P, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, _P, _S],
     "coco_allreduce": [_P, _P, _S],
     "coco_reduce_scatter": [_P, _P, _S],
     "coco_allgather": [_P, _P, _S],
@@ -104,7 +105,7 @@ _lib.coco_version.restype = ctypes.c_int
 _lib.coco_kernel_launches.restype = ctypes.c_uint64
 
 EXPORTED = [
-    "coco_fused_allreduce", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
+    "coco_fused_allreduce", "coco_fused_allreduce_at", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
     "coco_allreduce_rs_ag_noalloc",
     "coco_einsum", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs",
     "coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched", "coco_dropout_keep_mask",
@@ -195,6 +196,14 @@ def coco_fused_allreduce(partials, bias, residual, dropout_p, seed, out, stream=
     bias_ptr = None if bias is None else ctypes.c_void_p(bias.data_ptr())
     _check(_lib.coco_fused_allreduce(_ref(partials), bias_ptr, _ref(residual), float(dropout_p), int(seed),
                                      _ref(out), _stream(stream)), "coco_fused_allreduce")
+
+
+def coco_fused_allreduce_at(partials, bias, residual, dropout_p, seed, index_base, out, stream=None):
+    """coco_fused_allreduce over a contiguous part of larger tensors; index_base is the whole-tensor
+    row-major index of the part's first element (dropout indices and bias phase continue from it)."""
+    bias_ptr = None if bias is None else ctypes.c_void_p(bias.data_ptr())
+    _check(_lib.coco_fused_allreduce_at(_ref(partials), bias_ptr, _ref(residual), float(dropout_p), int(seed),
+                                        int(index_base), _ref(out), _stream(stream)), "coco_fused_allreduce_at")
 
 
 def coco_allreduce(inp, out, stream=None):

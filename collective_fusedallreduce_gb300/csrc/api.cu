@@ -315,9 +315,9 @@ COCO_EXPORT uint64_t coco_kernel_launches(void) { return g_launches.load(); }
 
 void coco::count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
-COCO_EXPORT coco_status coco_fused_allreduce(const coco_tensor* partials, const void* bias,
-                                             const coco_tensor* residual, float dropout_p, uint64_t seed,
-                                             const coco_tensor* out, void* stream) {
+static coco_status fused_allreduce_impl(const coco_tensor* partials, const void* bias,
+                                        const coco_tensor* residual, float dropout_p, uint64_t seed,
+                                        uint64_t index_base, const coco_tensor* out, void* stream) {
   TInfo in, o, res;
   coco_status st;
   if ((st = check_tensor(partials, &in)) != COCO_OK) return st;
@@ -334,6 +334,7 @@ COCO_EXPORT coco_status coco_fused_allreduce(const coco_tensor* partials, const 
   if (!(dropout_p >= 0.0f && dropout_p <= 1.0f)) return COCO_ERR_VALUE;  // also rejects NaN
   const int64_t H = in.local[in.ndim - 1];
   if (bias && (reinterpret_cast<uintptr_t>(bias) & 15)) return COCO_ERR_ALIGN;
+  if (index_base % static_cast<uint64_t>(16 / dtype_size(in.dtype))) return COCO_ERR_ALIGN;
   if (in.numel == 0) return COCO_OK;
 
   std::vector<Range> outs, ins;
@@ -363,7 +364,20 @@ COCO_EXPORT coco_status coco_fused_allreduce(const coco_tensor* partials, const 
   L.keep_threshold = static_cast<uint32_t>(std::floor(keep * 16777216.0));
   L.scale = dropout_p < 1.0f ? static_cast<float>(1.0 / keep) : 0.0f;
   L.seed = seed;
+  L.index_base = index_base;
   return cuda_status(launch_fused_allreduce(L, static_cast<cudaStream_t>(stream)));
+}
+
+COCO_EXPORT coco_status coco_fused_allreduce(const coco_tensor* partials, const void* bias,
+                                             const coco_tensor* residual, float dropout_p, uint64_t seed,
+                                             const coco_tensor* out, void* stream) {
+  return fused_allreduce_impl(partials, bias, residual, dropout_p, seed, 0, out, stream);
+}
+
+COCO_EXPORT coco_status coco_fused_allreduce_at(const coco_tensor* partials, const void* bias,
+                                                const coco_tensor* residual, float dropout_p, uint64_t seed,
+                                                uint64_t index_base, const coco_tensor* out, void* stream) {
+  return fused_allreduce_impl(partials, bias, residual, dropout_p, seed, index_base, out, stream);
 }
 
 COCO_EXPORT coco_status coco_allreduce(const coco_tensor* in, const coco_tensor* out, void* stream) {

@@ -36,6 +36,7 @@ struct FarLaunch {
   uint32_t keep_threshold;  // keep iff hash >> 40 < keep_threshold
   float scale;
   uint64_t seed;
+  uint64_t index_base;  // whole-tensor index of the first element (a multiple of the vector width)
 };
 cudaError_t launch_fused_allreduce(const FarLaunch& L, cudaStream_t s);
 

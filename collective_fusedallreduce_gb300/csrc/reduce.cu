@@ -119,10 +119,19 @@ struct FarArgs {
   int64_t nvec;          // vectors per rank
   const void* bias;      // nullptr = none
   int32_t bias_vecs;     // H / VEC
+  int32_t bias_phase;    // (index_base / VEC) mod bias_vecs: the bias vector of this launch's vector 0
+  uint64_t index_base;   // whole-tensor element index of this launch's element 0 (dropout)
   uint32_t threshold;
   float scale;
   uint64_t seed;
 };
+
+// The bias vector under vector v of this launch (bias broadcast over the last dimension).
+__device__ __forceinline__ int64_t bias_vector(int64_t v, const FarArgs& a) {
+  const int64_t x = v + a.bias_phase;
+  return x < (int64_t(1) << 31) ? static_cast<int64_t>(static_cast<uint32_t>(x) % static_cast<uint32_t>(a.bias_vecs))
+                                : x % a.bias_vecs;
+}
 
 // NR: compile-time rank count (0 = runtime, processed 8 at a time). Every
 // stream of a vector (the ranks' partials, the residual, the bias) is requested
@@ -158,9 +167,7 @@ __global__ void __launch_bounds__(kThreads, 3) k_fused_allreduce(const __grid_co
           if (vi[u] < a.nvec) raw[u][r] = ld_stream(static_cast<const char*>(in[r]) + vi[u] * 16);
         if (vi[u] < a.nvec && res) resv[u] = ld_stream(res + vi[u] * 16);
         if (vi[u] < a.nvec && bias) {
-          const int64_t bv = a.nvec < (int64_t(1) << 31)
-                                 ? static_cast<int64_t>(static_cast<uint32_t>(vi[u]) % static_cast<uint32_t>(a.bias_vecs))
-                                 : vi[u] % a.bias_vecs;
+          const int64_t bv = bias_vector(vi[u], a);
           biasv[u] = *reinterpret_cast<const uint4*>(bias + bv * 16);
         }
       }
@@ -208,17 +215,15 @@ __global__ void __launch_bounds__(kThreads, 3) k_fused_allreduce(const __grid_co
         if constexpr (NR > 0) {
           V::load(biasv[u], f);
         } else {
-          const int64_t bv = a.nvec < (int64_t(1) << 31)
-                                 ? static_cast<int64_t>(static_cast<uint32_t>(v) % static_cast<uint32_t>(a.bias_vecs))
-                                 : v % a.bias_vecs;
+          const int64_t bv = bias_vector(v, a);
           V::load(*reinterpret_cast<const uint4*>(bias + bv * 16), f);
         }
 #pragma unroll
         for (int j = 0; j < VE; ++j) acc[u][j] += f[j];
       }
       if constexpr (DROP) {
-        // state of element e = v*VE + j is seed + (e + 1) * gamma
-        uint64_t z = a.seed + (static_cast<uint64_t>(v) * VE + 1ull) * kGamma;
+        // state of whole-tensor element e = index_base + v*VE + j is seed + (e + 1) * gamma
+        uint64_t z = a.seed + (a.index_base + static_cast<uint64_t>(v) * VE + 1ull) * kGamma;
 #pragma unroll
         for (int j = 0; j < VE; ++j) {
           acc[u][j] = keep_state(z, a.threshold) ? acc[u][j] * a.scale : 0.0f;
@@ -476,6 +481,8 @@ cudaError_t launch_fused_allreduce(const FarLaunch& L, cudaStream_t s) {
   a.threshold = L.keep_threshold;
   a.scale = L.scale;
   a.seed = L.seed;
+  a.index_base = L.index_base;
+  a.bias_phase = static_cast<int32_t>((L.index_base / ve) % static_cast<uint64_t>(a.bias_vecs));
   switch (L.dtype) {
     case COCO_F32:
       return L.dropout ? far_typed<float, true>(a, L.nranks, L.ngroups, s) : far_typed<float, false>(a, L.nranks, L.ngroups, s);

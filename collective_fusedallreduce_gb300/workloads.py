@@ -6,6 +6,9 @@ libcoco; every arithmetic step runs in the library's kernels.
 * ``megatron_attention_tail``: [CoCoNet] Fig. 3 -- the local MatMul of two
   tensors sliced on the contracting dimension, then FusedAllReduce with bias,
   dropout and residual.
+* ``megatron_attention_tail_overlap``: the same with [CoCoNet] §5.3's Overlap
+  construct in row chunks (FusedAllReduce of one chunk beside the MatMul of
+  the next, on two streams).
 * ``mlp_1d``: the 1-D partitioned two-layer MLP of [Decomp] §2.2 Fig. 2
   (Looped AllGather-Einsum case 1, then Looped Einsum-ReduceScatter).
 * ``mlp_2d``: the [M, N]-mesh two-layer MLP of [Decomp] §2.2 Fig. 3:
@@ -39,6 +42,41 @@ def megatron_attention_tail(in_slices, w_slices, bias, residual, p, seed, layer=
     coco.coco_einsum("mk,kn->mn", coco.sliced(in_slices, 1), coco.sliced(w_slices, 0), coco.local(layer), stream)
     coco.coco_fused_allreduce(coco.local(layer), bias, None if residual is None else coco.replicated([residual] * n),
                               p, seed, coco.replicated(out), stream)
+    return layer, out
+
+
+def megatron_attention_tail_overlap(in_slices, w_slices, bias, residual, p, seed, chunks, layer=None, out=None,
+                                    stream=None, side_stream=None):
+    """The same tail with [CoCoNet] §5.3's Overlap construct, in chunks: the rows are cut into
+    ``chunks`` ranges; the MatMul of each range runs on ``stream`` and its FusedAllReduce on
+    ``side_stream`` as soon as that range's partials exist, so the FusedAllReduce of one range runs
+    while the MatMul computes the next. Ordering is by CUDA events only (nothing waits on the device).
+    The FusedAllReduce of a range passes the range's whole-tensor index base, so the result equals
+    ``megatron_attention_tail``'s bit for bit. ``stream`` waits for the last FusedAllReduce before
+    returning. Returns (layer, out)."""
+    n = len(in_slices)
+    rows, h = in_slices[0].shape[0], w_slices[0].shape[1]
+    dt, dev = in_slices[0].dtype, in_slices[0].device
+    layer = layer if layer is not None else [_empty((rows, h), dt, dev) for _ in range(n)]
+    out = out if out is not None else [_empty((rows, h), dt, dev) for _ in range(n)]
+    main = stream if stream is not None else torch.cuda.current_stream(dev)
+    side = side_stream if side_stream is not None else torch.cuda.Stream(device=dev)
+    chunks = max(1, min(int(chunks), rows))
+    bounds = [rows * c // chunks for c in range(chunks + 1)]
+    for r0, r1 in zip(bounds[:-1], bounds[1:]):
+        if r1 == r0:
+            continue
+        coco.coco_einsum("mk,kn->mn", coco.sliced([x[r0:r1] for x in in_slices], 1), coco.sliced(w_slices, 0),
+                         coco.local([x[r0:r1] for x in layer]), main)
+        ready = torch.cuda.Event()
+        ready.record(main)
+        side.wait_event(ready)
+        coco.coco_fused_allreduce_at(coco.local([x[r0:r1] for x in layer]), bias,
+                                     None if residual is None else coco.replicated([residual[r0:r1]] * n),
+                                     p, seed, r0 * h, coco.replicated([x[r0:r1] for x in out]), side)
+    done = torch.cuda.Event()
+    done.record(side)
+    main.wait_event(done)
     return layer, out
 
 

@@ -122,6 +122,21 @@ coco_status coco_fused_allreduce(const coco_tensor* partials, const void* bias,
                                  const coco_tensor* out, void* stream);
 
 /*
+ * The same FusedAllReduce over a contiguous part of larger tensors, for the
+ * chunked form of [CoCoNet]'s Overlap construct (§5.3, Fig. 9: the AllReduce
+ * of a chunk runs while the MatMul produces the next one). index_base is the
+ * row-major index, inside one rank's whole tensor, of the first element of
+ * the part passed; dropout element indices and the bias phase continue from
+ * it, so calls over consecutive parts give, bit for bit, the result of one
+ * coco_fused_allreduce over the whole. index_base must be a multiple of
+ * 16 / sizeof(T) elements (else COCO_ERR_ALIGN); coco_fused_allreduce is
+ * index_base = 0. Everything else as coco_fused_allreduce.
+ */
+coco_status coco_fused_allreduce_at(const coco_tensor* partials, const void* bias,
+                                    const coco_tensor* residual, float dropout_p, uint64_t seed,
+                                    uint64_t index_base, const coco_tensor* out, void* stream);
+
+/*
  * Plain AllReduce ([Decomp] §2.1): out_q = sum_r in_r (fp32 sum in rank order
  * 0..N-1, one rounding), for every rank q. in LOCAL, out REPLICATED, same
  * dtype and shape. In place (out_q == in_q exactly) is allowed.

@@ -106,6 +106,27 @@ def test_far_validation(coco):
     assert far(coco, good_in, good_out, residual=mk(coco, F16, R, (8, 16), 2, base=FAKE + (1 << 42))) == 2
 
 
+def test_far_at_index_base_validation(coco):
+    """coco_fused_allreduce_at: index_base must be a multiple of the 16-byte vector width in elements;
+    the other checks are coco_fused_allreduce's."""
+    F16, F32, L, R = coco.F16, coco.F32, coco.LOCAL, coco.REPLICATED
+
+    def far_at(dtype, base, p=0.0):
+        ins = mk(coco, dtype, L, (4, 16), 2)
+        outs = mk(coco, dtype, R, (4, 16), 2, base=FAKE + (1 << 40))
+        return coco.raw_call("coco_fused_allreduce_at", ctypes.byref(ins), None, None, p, 0, base,
+                             ctypes.byref(outs), None)
+
+    assert far_at(F16, 4) == 5   # 16-bit: multiples of 8 elements
+    assert far_at(F16, 12) == 5
+    assert far_at(F32, 2) == 5   # fp32: multiples of 4
+    assert far_at(F16, 16, p=2.0) == 10  # the shared checks still apply
+    empty_in = mk(coco, F16, L, (0, 16), 2)
+    empty_out = mk(coco, F16, R, (0, 16), 2, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_fused_allreduce_at", ctypes.byref(empty_in), None, None, 0.1, 0, 8 * 1000,
+                         ctypes.byref(empty_out), None) == 0
+
+
 def test_far_aliasing(coco):
     F16, L, R = coco.F16, coco.LOCAL, coco.REPLICATED
     nbytes = 4 * 16 * 2

@@ -57,6 +57,51 @@ def test_fused_allreduce_matches_oracle(coco, dtype, n, shape):
         assert torch.equal(o, outs[0])  # replicated: bitwise identical on every rank
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_fused_allreduce_at_row_chunks_equal_the_whole_call(coco, dtype):
+    """[CoCoNet] §5.3 Overlap in chunks: FusedAllReduce over consecutive row ranges with the ranges'
+    whole-tensor index bases gives, bit for bit, the one-call result (dropout mask included)."""
+    n, rows, h, p, seed = 4, 40, 64, 0.3, 77
+    parts = dev(synth.per_rank(31, 0, n, (rows, h), dtype, "uniform"))
+    b = synth.tensor(synth.seed_of(31, 1), (h,), dtype, "uniform").cuda()
+    r = synth.tensor(synth.seed_of(31, 2), (rows, h), dtype, "uniform").cuda()
+    whole = empty_like_list(n, (rows, h), dtype)
+    coco.coco_fused_allreduce(coco.local(parts), b, coco.replicated([r] * n), p, seed, coco.replicated(whole))
+    chunked = empty_like_list(n, (rows, h), dtype)
+    for r0, r1 in [(0, 8), (8, 24), (24, 40)]:
+        coco.coco_fused_allreduce_at(coco.local([x[r0:r1] for x in parts]), b, coco.replicated([r[r0:r1]] * n), p,
+                                     seed, r0 * h, coco.replicated([o[r0:r1] for o in chunked]))
+    torch.cuda.synchronize()
+    for q in range(n):
+        assert torch.equal(chunked[q], whole[q])
+    ref = oracle.fused_allreduce([f64(x) for x in parts], f64(b), f64(r), p, seed)
+    assert_close(chunked[0], ref, dtype, "chunked")
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_fused_allreduce_at_keeps_the_bias_phase_off_a_row_boundary(coco, dtype):
+    """A part that starts mid-row (index_base not a multiple of the row length) still takes bias
+    element (e mod H) and dropout index e of the whole tensor."""
+    n, rows, h, p, seed, off, m = 3, 16, 64, 0.2, 5, 8, 4
+    parts = dev(synth.per_rank(32, 0, n, (rows, h), dtype, "uniform"))
+    b = synth.tensor(synth.seed_of(32, 1), (h,), dtype, "uniform").cuda()
+    r = synth.tensor(synth.seed_of(32, 2), (rows, h), dtype, "uniform").cuda()
+    whole = empty_like_list(n, (rows, h), dtype)
+    coco.coco_fused_allreduce(coco.local(parts), b, coco.replicated([r] * n), p, seed, coco.replicated(whole))
+
+    def part(t):
+        return t.reshape(-1)[off:off + m * h].view(m, h)
+
+    outs = empty_like_list(n, (m, h), dtype)
+    coco.coco_fused_allreduce_at(coco.local([part(x) for x in parts]), b, coco.replicated([part(r)] * n), p, seed,
+                                 off, coco.replicated(outs))
+    torch.cuda.synchronize()
+    for q in range(n):
+        assert torch.equal(outs[q], part(whole[q]))
+    ref = oracle.fused_allreduce([f64(x) for x in parts], f64(b), f64(r), p, seed).reshape(-1)[off:off + m * h]
+    assert_close(outs[0], ref.reshape(m, h), dtype, "mid-row part")
+
+
 @pytest.mark.parametrize("bias,res,p", [(False, False, 0.0), (True, False, 0.0), (False, True, 0.5),
                                         (True, True, 0.0), (False, False, 0.3), (True, True, 1.0)])
 def test_fused_allreduce_optional_parts(coco, bias, res, p):

@@ -67,6 +67,27 @@ def test_megatron_tail_chain_small(coco, workloads, dtype):
         assert_close(o, ref, dtype, f"rank {q}")
 
 
+@pytest.mark.parametrize("chunks", [1, 3, 4, 7])
+def test_megatron_tail_overlap_equals_the_unchunked_chain(coco, workloads, chunks):
+    """[CoCoNet] §5.3 Overlap in row chunks on two streams: bit for bit the unchunked chain's
+    partials and outputs (the chunks' FusedAllReduces continue the dropout index)."""
+    n, rows, hidden = 8, 264, 512
+    ins = dev(synth.per_rank(2, 20, n, (rows, hidden // n), F16))
+    ws = dev(synth.per_rank(2, 21, n, (hidden // n, hidden), F16, std=0.02))
+    bias = synth.tensor(synth.seed_of(2, 22), (hidden,), F16, std=0.02).cuda()
+    res = synth.tensor(synth.seed_of(2, 23), (rows, hidden), F16).cuda()
+    layer_a, out_a = workloads.megatron_attention_tail(ins, ws, bias, res, 0.1, 9)
+    side = torch.cuda.Stream()
+    layer_b = out_b = None
+    for _ in range(2):  # twice: the second call reuses the buffers the first one's side stream wrote
+        layer_b, out_b = workloads.megatron_attention_tail_overlap(ins, ws, bias, res, 0.1, 9, chunks, layer_b, out_b,
+                                                                   side_stream=side)
+    coco.coco_device_status()
+    for q in range(n):
+        assert torch.equal(layer_a[q], layer_b[q])
+        assert torch.equal(out_a[q], out_b[q])
+
+
 @pytest.mark.parametrize("m_x,n_y", [(2, 4), (1, 2), (2, 1)])
 def test_mesh_2d_mlp_small(coco, workloads, m_x, n_y):
     b, f, h = 64 * n_y, 64 * m_x * n_y, 128 * m_x
