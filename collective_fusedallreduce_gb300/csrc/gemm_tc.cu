@@ -34,7 +34,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -932,6 +934,19 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
   if (!encode_fn()) return cudaErrorNotSupported;
   const bool far = plan.mode == EPI_FUSED_ALLREDUCE;
   if (far && plan.out_dtype == COCO_F32) return cudaErrorNotSupported;
+  // Every job (one output region's whole K-segment loop) must fit one launch's parameter block:
+  // checked for all jobs before anything is launched, so an unsupported plan runs nothing.
+  for (const Job& J : plan.jobs) {
+    std::vector<int> as, bs;
+    for (int k = 0; k < J.nseg; ++k) {
+      const Seg& S = plan.segs[J.seg0 + k];
+      if (std::find(as.begin(), as.end(), S.a) == as.end()) as.push_back(S.a);
+      if (std::find(bs.begin(), bs.end(), S.b) == bs.end()) bs.push_back(S.b);
+    }
+    if (static_cast<int>(as.size() + bs.size()) > MAX_MAPS || J.nseg > MAX_SEGS ||
+        J.nout + (far && J.res ? 1 : 0) > MAX_OUTS)
+      return cudaErrorNotSupported;
+  }
   // k-blocks per tile, averaged over the plan's jobs
   int64_t kb_sum = 0;
   for (const Job& J : plan.jobs)

@@ -246,6 +246,12 @@ coco_status coco_scattered_allreduce(const coco_scattered_plan* plan, float alph
  * tensor cores with fp32 accumulation; F32 runs on fp32 FMA units. The output
  * dtype is out->dtype (F32, F16 or BF16), rounded once from the fp32
  * accumulator.
+ *
+ * Tensor-core limit: the loop that produces one output region (its K-segments:
+ * the N rank slices of case 2, of the Einsum-ReduceScatter and of the fused
+ * MatMul) must fit one launch's parameter block, at most 80 distinct operand
+ * views (two per rank slice, so N <= 40 for those forms) and 192 K-segments.
+ * Larger requests return COCO_ERR_UNSUPPORTED before anything is launched.
  */
 
 /*

@@ -259,3 +259,33 @@ def test_config5b_allreduce_rs_ag_full_size(coco):
     assert_close(direct[idx], ref, torch.float32)
     del ins, outs, scratch
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("n,g", [(64, 1), (16, 4), (9, 7)])
+def test_at_the_pointer_limit(coco, n, g):
+    """nranks x ngroups up to the interface's 64 pointers: FusedAllReduce (the runtime rank-count path,
+    8 ranks at a time), ReduceScatter and AllGather."""
+    dtype, shape = torch.float16, (8, 64)
+    parts = dev(synth.per_rank(33, 0, n * g, shape, dtype, "uniform"))
+    bias = synth.tensor(synth.seed_of(33, 1), (64,), dtype, "uniform").cuda()
+    outs = empty_like_list(n * g, shape, dtype)
+    coco.coco_fused_allreduce(coco.local(parts, ngroups=g), bias, None, 0.25, 11, coco.replicated(outs, ngroups=g))
+    torch.cuda.synchronize()
+    for gi in range(g):
+        ref = oracle.fused_allreduce([f64(x) for x in parts[gi * n:(gi + 1) * n]], f64(bias), None, 0.25, 11)
+        for q in range(n):
+            assert_close(outs[gi * n + q], ref, dtype, f"group {gi} rank {q}")
+    rs_shape = (n * 2, 16)
+    ins = dev(synth.per_rank(34, 0, n * g, rs_shape, torch.float32, "uniform"))
+    scat = empty_like_list(n * g, (2, 16), torch.float32)
+    coco.coco_reduce_scatter(coco.local(ins, ngroups=g), coco.sliced(scat, 0, ngroups=g))
+    full = empty_like_list(n * g, rs_shape, torch.float32)
+    coco.coco_allgather(coco.sliced(scat, 0, ngroups=g), coco.replicated(full, ngroups=g))
+    torch.cuda.synchronize()
+    for gi in range(g):
+        ref = oracle.reduce_scatter([f64(x) for x in ins[gi * n:(gi + 1) * n]], 0)
+        for r in range(n):
+            assert_close(scat[gi * n + r], ref[r], torch.float32, f"group {gi} slice {r}")
+        want = torch.cat([s.cpu() for s in scat[gi * n:(gi + 1) * n]], 0)
+        for q in range(n):
+            assert torch.equal(full[gi * n + q].cpu(), want)

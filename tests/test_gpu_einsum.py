@@ -211,3 +211,41 @@ def test_zero_contraction_gives_zeros(coco):
     torch.cuda.synchronize()
     for o in outs:
         assert torch.count_nonzero(o) == 0
+
+
+@pytest.mark.parametrize("n,g", [(64, 1), (32, 2), (40, 1)])
+def test_looped_einsums_at_the_pointer_limit(coco, n, g):
+    """Up to 64 ranks (or 32 x 2 groups): the planner spreads the N x N (rank, step) jobs of case 1 and
+    their operand maps over several launches. The einsum-ReduceScatter sums N rank slices per output
+    region, two operand views each, which one launch holds up to N = 40; beyond that the call returns
+    COCO_ERR_UNSUPPORTED and launches nothing."""
+    ms, k, nn = 16, 64, 64
+    shards = gen(40, 0, n * g, (ms, k), BF16, std=k ** -0.5)
+    rhs = gen(40, 1, n * g, (k, nn), BF16)
+    outs = empty_like_list(n * g, (n * ms, nn), BF16)
+    coco.coco_looped_ag_einsum("mk,kn->mn", coco.sliced(dev(shards), 0, ngroups=g), coco.local(dev(rhs), ngroups=g),
+                               coco.local(outs, ngroups=g))
+    for gi in range(g):
+        sl = slice(gi * n, (gi + 1) * n)
+        refs = oracle.allgather_einsum("mk,kn->mn", "lhs", "m", [f64(s) for s in shards[sl]],
+                                       [f64(x) for x in rhs[sl]])
+        check(coco, outs[sl], refs, BF16, f"case 1 group {gi}")
+    ks = 16
+    lhs = gen(41, 0, n * g, (ms, ks), BF16, std=(n * ks) ** -0.5)
+    rw = gen(41, 1, n * g, (ks, n * 8), BF16)
+    ys = empty_like_list(n * g, (ms, 8), BF16)
+    if n > 40:
+        with pytest.raises(coco.CocoError) as exc:
+            coco.coco_looped_einsum_rs("mk,kn->mn", coco.sliced(dev(lhs), 1, ngroups=g),
+                                       coco.sliced(dev(rw), 0, ngroups=g), coco.sliced(ys, 1, ngroups=g))
+        assert exc.value.name == "COCO_ERR_UNSUPPORTED"
+        torch.cuda.synchronize()
+        assert all(torch.isnan(y).all() for y in ys)  # nothing ran
+        return
+    coco.coco_looped_einsum_rs("mk,kn->mn", coco.sliced(dev(lhs), 1, ngroups=g), coco.sliced(dev(rw), 0, ngroups=g),
+                               coco.sliced(ys, 1, ngroups=g))
+    for gi in range(g):
+        sl = slice(gi * n, (gi + 1) * n)
+        refs = oracle.einsum_reduce_scatter("mk,kn->mn", [f64(x) for x in lhs[sl]], [f64(x) for x in rw[sl]], "n")
+        check(coco, ys[sl], refs, BF16, f"einsum-RS group {gi}")
+
