@@ -80,7 +80,7 @@ struct Cfg {
 // dominates and the two CTAs are better left independent.
 constexpr int kTwoSmMinKBlocks = 4;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int GROUP_M = 16;  // tile rasterisation: 16 m-tiles per group, n-major inside
+constexpr int GROUP_M = 16;  // tile rasterisation for large B operands: 16 m-tiles per group, n-major inside
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 constexpr int MAX_MAPS = 80;
@@ -96,6 +96,7 @@ struct TcParams {
   OutView outs[MAX_OUTS];
   int32_t unit_start[MAX_JOBS + 1];  // first work unit (a pair of vertically adjacent tiles) of each job
   int32_t njobs;
+  int32_t group_pairs;  // rasterisation: pairs of m-tiles per group, n-major inside a group
   int32_t total_units;
   uint32_t idesc;
   int32_t out_dtype;
@@ -361,7 +362,7 @@ struct Tile {
 
 // Work unit u is a pair of vertically adjacent 128 x 256 tiles with the same
 // column block; CTA `rank` of the cluster takes m-tile 2 * pair + rank. Units
-// are rasterised in groups of GROUP_M / 2 pairs, column-major inside a group.
+// are rasterised in groups of P.group_pairs pairs, column-major inside a group.
 __device__ __forceinline__ Tile decode_unit(const TcParams& P, int u, int rank) {
   int lo = 0, hi = P.njobs - 1;
   while (lo < hi) {  // last job with unit_start <= u
@@ -372,7 +373,7 @@ __device__ __forceinline__ Tile decode_unit(const TcParams& P, int u, int rank) 
   const int mpairs = (jm + 2 * BM - 1) / (2 * BM), ntiles = (jn + BN - 1) / BN;
   const int local = u - P.unit_start[lo];
   const int per_b = mpairs * ntiles;
-  constexpr int GP = GROUP_M / 2;
+  const int GP = P.group_pairs;
   Tile T;
   T.job = lo;
   T.bb = local / per_b;
@@ -1052,6 +1053,20 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
     if (njobs == 0) { status = cudaErrorInvalidValue; break; }  // a single job exceeds the limits
     P->unit_start[njobs] = tiles;
     P->njobs = njobs;
+    {
+      // When the largest job's whole B operand fits in half of L2, walk each job one pair of
+      // m-tiles at a time across all its n-tiles: B stays in L2 while A streams past once, which
+      // cut DRAM reads and, under the power cap, bought clock (case 1: 1% faster sustained).
+      // Otherwise groups of GROUP_M m-tiles share both operands' slices within a wave.
+      int64_t bmax = 0;
+      for (int q = 0; q < njobs; ++q) {
+        int64_t b = 0;
+        for (int k = 0; k < P->jobs[q].nseg; ++k)
+          b += static_cast<int64_t>(P->segs[P->jobs[q].seg0 + k].klen) * P->jobs[q].n * 2;
+        bmax = b > bmax ? b : bmax;
+      }
+      P->group_pairs = bmax <= (int64_t(64) << 20) ? 1 : GROUP_M / 2;
+    }
     P->total_units = tiles;
     P->idesc = idesc;
     P->out_dtype = plan.out_dtype;
