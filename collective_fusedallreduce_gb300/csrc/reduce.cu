@@ -7,12 +7,12 @@
 // Communication) and Fig. 3; [Decomp] "Overlap Communication with Dependent
 // Computation via Decomposition in Large Deep Learning Models", §2.1.
 //
-// Design (HBM-bound streaming): every thread moves 16-byte vectors; a block
-// handles U vectors per thread per iteration, laid out so each warp access is
-// a fully coalesced 512-byte run; all N loads of an iteration are issued
-// before the first add so ~N*U*16 bytes are in flight per thread; sums run in
-// fp32 in rank order 0..N-1 and each output is rounded once. Grids are a
-// multiple of the SM count and stride over the data.
+// Design (HBM-bound streaming): every thread moves 16-byte vectors, so each
+// warp access is a fully coalesced 512-byte run; all N loads of a vector (and
+// its residual and bias) are issued before the first add; sums run in fp32 in
+// rank order 0..N-1 and each output is rounded once. Grids have one 256-thread
+// block per 256 vectors (many short blocks kept HBM busier than a few resident
+// blocks per SM) and stride over the data beyond 2^20 blocks.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
