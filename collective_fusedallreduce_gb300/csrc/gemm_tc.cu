@@ -1054,18 +1054,21 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
     P->unit_start[njobs] = tiles;
     P->njobs = njobs;
     {
-      // When the largest job's whole B operand fits in half of L2, walk each job one pair of
-      // m-tiles at a time across all its n-tiles: B stays in L2 while A streams past once, which
-      // cut DRAM reads and, under the power cap, bought clock (case 1: 1% faster sustained).
-      // Otherwise groups of GROUP_M m-tiles share both operands' slices within a wave.
+      // Long k-loops (64 or more k-blocks) whose largest whole B operand fits in half of L2 walk
+      // each job one pair of m-tiles at a time across all its n-tiles: B stays in L2 while A
+      // streams past once, which cut DRAM reads and, under the power cap, bought clock (case 1:
+      // 1% faster sustained). Otherwise groups of GROUP_M m-tiles share both operands' slices
+      // within a wave (1% faster on the K = 512 MatMul).
       int64_t bmax = 0;
+      int kbmin = 1 << 30;
       for (int q = 0; q < njobs; ++q) {
         int64_t b = 0;
         for (int k = 0; k < P->jobs[q].nseg; ++k)
           b += static_cast<int64_t>(P->segs[P->jobs[q].seg0 + k].klen) * P->jobs[q].n * 2;
         bmax = b > bmax ? b : bmax;
+        kbmin = P->jobs[q].kblocks < kbmin ? P->jobs[q].kblocks : kbmin;
       }
-      P->group_pairs = bmax <= (int64_t(64) << 20) ? 1 : GROUP_M / 2;
+      P->group_pairs = (bmax <= (int64_t(64) << 20) && kbmin >= 64) ? 1 : GROUP_M / 2;
     }
     P->total_units = tiles;
     P->idesc = idesc;
