@@ -86,6 +86,7 @@ for _name, _args in {
     "coco_looped_einsum_rs_sched": [ctypes.c_char_p, _P, _P, _P, ctypes.c_int, _S],
     "coco_dropout_keep_mask": [ctypes.c_uint64, ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p, _S],
     "coco_device_status": [_S],
+    "coco_wait_selftest": [ctypes.c_uint64, _S],
 }.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
@@ -110,7 +111,7 @@ EXPORTED = [
     "coco_einsum", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs",
     "coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched", "coco_dropout_keep_mask",
     "coco_scattered_table_bytes", "coco_scattered_table_build", "coco_scattered_allreduce",
-    "coco_device_status", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
+    "coco_device_status", "coco_wait_selftest", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
 ]
 
 
@@ -266,6 +267,12 @@ def coco_dropout_keep_mask(seed, dropout_p, first_index, count, mask, stream=Non
 
 def coco_device_status(stream=None):
     _check(_lib.coco_device_status(_stream(stream)), "coco_device_status")
+
+
+def coco_wait_selftest(timeout_ns, stream=None):
+    """Launches the failure-path self-test: a bounded wait on a barrier nothing completes
+    (``timeout_ns`` limit); the next coco_device_status raises COCO_ERR_TIMEOUT."""
+    _check(_lib.coco_wait_selftest(int(timeout_ns), _stream(stream)), "coco_wait_selftest")
 
 
 def raw_call(name, *args):

@@ -584,6 +584,13 @@ COCO_EXPORT coco_status coco_dropout_keep_mask(uint64_t seed, float dropout_p, u
   return cuda_status(launch_keep_mask(seed, threshold, first_index, count, mask, static_cast<cudaStream_t>(stream)));
 }
 
+COCO_EXPORT coco_status coco_wait_selftest(uint64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1000ull || timeout_ns > 1000000000ull) return COCO_ERR_VALUE;
+  unsigned int* err = gemm_error_word();
+  if (!err) return cuda_status(cudaErrorSymbolNotFound);
+  return cuda_status(launch_wait_selftest(timeout_ns, static_cast<cudaStream_t>(stream), err));
+}
+
 COCO_EXPORT coco_status coco_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_status(e);

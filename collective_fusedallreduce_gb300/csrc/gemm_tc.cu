@@ -142,13 +142,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait. Returns false on timeout or when another role aborted.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            uint64_t timeout_ns = kTimeoutNs) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
     if ((it & 31) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kTimeoutNs) return false;
+      if (globaltimer() - t0 > timeout_ns) return false;
     }
   }
 }
@@ -159,10 +160,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // The same for a whole warp, with one answer for all its lanes. Only lane 0
 // polls a phase that is not complete yet; the lanes that issue async
 // operations afterwards are lane 0 (the elected lane of a converged warp).
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               uint64_t timeout_ns = kTimeoutNs) {
   if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait_slow(bar, parity, abort_flag);
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_slow(bar, parity, abort_flag, timeout_ns);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 // One lane of a converged warp (the lowest), chosen by the hardware.
@@ -861,6 +863,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
   }
 }
 
+// Failure-path self-test: the TMEM owner allocates, a consumer warp waits for a
+// phase that nothing completes, with the same bounded wait as the GEMM's roles
+// but a caller-chosen limit; on expiry it records COCO_ERR_TIMEOUT and raises
+// the abort flag, and the owner frees TMEM before every thread returns.
+__global__ void __launch_bounds__(64, 1) k_wait_selftest(unsigned int* err, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc<false>(smem_u32(&tslot), 32);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tslot;
+  if (warp == 1) {
+    const bool ok = mbar_wait_warp(smem_u32(&bar), 0, abort_flag, timeout_ns);
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      atomicCAS(err, 0u, static_cast<unsigned int>(COCO_ERR_TIMEOUT));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc<false>(tmem, 32);
+  }
+}
+
 // ------------------------------------------------------------------- host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -1087,6 +1124,12 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
   }
   delete P;
   return status;
+}
+
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, unsigned int* err_word) {
+  k_wait_selftest<<<1, 64, 0, s>>>(err_word, timeout_ns);
+  count_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace coco

@@ -138,6 +138,8 @@ cudaError_t launch_gemm_simt(const GemmPlan& plan, cudaStream_t s);
 
 // Device error word of the GEMM kernels (bounded waits record here).
 unsigned int* gemm_error_word();
+// One CTA waits on a barrier nothing completes, bounded by timeout_ns (the failure-path self-test).
+cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, unsigned int* err_word);
 
 int sm_count();
 

@@ -366,6 +366,18 @@ coco_status coco_dropout_keep_mask(uint64_t seed, float dropout_p, uint64_t firs
 coco_status coco_device_status(void* stream);
 
 /*
+ * Self-test of the device-side failure path (no counterpart on the pages):
+ * one CTA allocates tensor memory, then one warp waits on an mbarrier phase
+ * that nothing completes, with the bounded wait the tensor-core kernels use but
+ * a limit of timeout_ns (1e3 .. 1e9 ns, else COCO_ERR_VALUE) on %globaltimer.
+ * When the limit passes, the kernel records COCO_ERR_TIMEOUT and raises its
+ * abort flag, the owner frees the tensor memory, and every thread returns: the
+ * next coco_device_status() reports COCO_ERR_TIMEOUT (once) and the context
+ * stays usable. Nothing faults, traps or hangs.
+ */
+coco_status coco_wait_selftest(uint64_t timeout_ns, void* stream);
+
+/*
  * Number of kernels this library has launched in this process so far (all
  * threads, all devices). Launch accounting for benchmarks and tests.
  */

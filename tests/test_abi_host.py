@@ -127,6 +127,11 @@ def test_far_at_index_base_validation(coco):
                          ctypes.byref(empty_out), None) == 0
 
 
+def test_wait_selftest_limit_validation(coco):
+    for bad in (0, 999, 1_000_000_001, 2 ** 63):
+        assert coco.raw_call("coco_wait_selftest", bad, None) == 10
+
+
 def test_far_aliasing(coco):
     F16, L, R = coco.F16, coco.LOCAL, coco.REPLICATED
     nbytes = 4 * 16 * 2
