@@ -289,3 +289,36 @@ def test_at_the_pointer_limit(coco, n, g):
         want = torch.cat([s.cpu() for s in scat[gi * n:(gi + 1) * n]], 0)
         for q in range(n):
             assert torch.equal(full[gi * n + q].cpu(), want)
+
+
+@pytest.mark.slow
+def test_fused_allreduce_beyond_32_bit_element_indices(coco):
+    """A tensor of 2^31 + 4096 fp16 elements per rank (4 GiB): element offsets, dropout indices and
+    the bias phase past 2^31 are 64-bit. Sampled rows near the start, across the 2^31 boundary and at
+    the end match the oracle evaluated at their whole-tensor indices; the mask there is bit-exact."""
+    n, h = 2, 4096
+    rows = (1 << 31) // h + 1
+    g = torch.Generator(device="cuda")
+    parts = []
+    for r in range(n):
+        x = torch.empty((rows, h), dtype=torch.float16, device="cuda")
+        g.manual_seed(synth.seed_of(36, 0, r))
+        x.uniform_(-1, 1, generator=g)
+        parts.append(x)
+    bias = synth.tensor(synth.seed_of(36, 1), (h,), torch.float16, "uniform").cuda()
+    res = torch.empty((rows, h), dtype=torch.float16, device="cuda")
+    g.manual_seed(synth.seed_of(36, 2))
+    res.uniform_(-1, 1, generator=g)
+    out = torch.empty((rows, h), dtype=torch.float16, device="cuda")
+    coco.coco_fused_allreduce(coco.local(parts), bias, coco.replicated([res] * n), 0.5, 99, coco.replicated([out] * n))
+    coco.coco_device_status()
+    sample = np.array([0, 1, rows // 2, rows - 3, rows - 2, rows - 1])
+    idx = sample[:, None].astype(np.uint64) * np.uint64(h) + np.arange(h, dtype=np.uint64)[None, :]
+    assert int(idx.max()) >= (1 << 31)
+    ref = oracle.fused_allreduce([f64(x[sample]) for x in parts], f64(bias), f64(res[sample]), 0.5, 99, index=idx)
+    got = out[torch.from_numpy(sample).cuda()]
+    assert_close(got, ref, torch.float16, "rows past 2^31")
+    keep = oracle.keep_mask(99, 0.5, idx.ravel()).reshape(idx.shape)
+    dropped = torch.from_numpy(~keep).cuda()
+    assert torch.equal(got[dropped], res[torch.from_numpy(sample).cuda()][dropped])
+    del parts, res, out
