@@ -41,8 +41,20 @@ def _stale(obj, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose=False, ptxas_verbose=False, force=False):
-    """Compile (only what changed) and link libcoco.so. Returns the library path."""
+# Host-side sanitizers for a checking build of the library (device code is unchanged).
+# (nvcc splits -Xcompiler values at commas, so every flag is passed on its own)
+SANITIZE = ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined", "-Xcompiler",
+            "-fno-omit-frame-pointer", "-Xcompiler", "-fno-sanitize-recover=all"]
+
+
+def build(verbose=False, ptxas_verbose=False, force=False, build_dir=None, lib=None, extra=()):
+    """Compile (only what changed) and link libcoco.so. Returns the library path.
+
+    ``build_dir`` / ``lib`` / ``extra`` build a variant elsewhere with extra nvcc flags (see
+    build_sanitized); the default is the in-tree library."""
+    BUILD = build_dir or globals()["BUILD"]
+    LIB = lib or globals()["LIB"]
+    extra = list(extra)
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
@@ -53,7 +65,7 @@ def build(verbose=False, ptxas_verbose=False, force=False):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or ptxas_verbose or _stale(obj, [src] + headers):
-            cmd = [cc] + ARCH + FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", src, "-o", obj]
+            cmd = [cc] + ARCH + FLAGS + extra + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", src, "-o", obj]
             jobs.append(cmd)
 
     def run(cmd):
@@ -69,7 +81,7 @@ def build(verbose=False, ptxas_verbose=False, force=False):
                     raise RuntimeError(f"nvcc failed on {cmd[-3]}")
     if jobs or not os.path.exists(LIB):
         tmp = LIB + ".tmp"
-        cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
+        cmd = [cc] + ARCH + extra + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode:
             sys.stderr.write(" ".join(cmd) + "\n" + p.stdout + p.stderr)
@@ -81,3 +93,18 @@ def build(verbose=False, ptxas_verbose=False, force=False):
 if __name__ == "__main__":
     build(verbose="-v" in sys.argv, ptxas_verbose="--ptxas" in sys.argv, force="--force" in sys.argv)
     print(LIB)
+
+
+def build_sanitized(dest_dir):
+    """The same library with AddressSanitizer and UndefinedBehaviorSanitizer in its host code, built
+    under ``dest_dir``. A process loads it with the ASan runtime preloaded (sanitizer_runtime()) and
+    COCO_LIBRARY pointing at it. Returns the library path."""
+    return build(build_dir=os.path.join(dest_dir, "_build"), lib=os.path.join(dest_dir, "libcoco_sanitized.so"),
+                 extra=SANITIZE)
+
+
+def sanitizer_runtime():
+    """Path of the ASan runtime that must be preloaded into a process loading the sanitized build."""
+    p = subprocess.run(["gcc", "-print-file-name=libasan.so"], capture_output=True, text=True)
+    return p.stdout.strip()
+

@@ -18,7 +18,8 @@ import os
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoco.so")
+# COCO_LIBRARY selects another build of the same library (e.g. build.build_sanitized's).
+_LIB_PATH = os.environ.get("COCO_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "libcoco.so")
 if not os.path.exists(_LIB_PATH):
     raise ImportError(f"{_LIB_PATH} is missing: build it with __graft_entry__.build()")
 _lib = ctypes.CDLL(_LIB_PATH)
