@@ -483,6 +483,7 @@ class Mesh2D(Workload):
         self.bufs = None
         from collective_fusedallreduce_gb300 import workloads
         self.bufs = workloads.mlp_2d(self.x, self.w1, self.w2, m_x, n_y)  # allocates buffers
+        self.side = torch.cuda.Stream(device=dev)  # the AllGather of W2 runs beside the first einsum
         self.config = {"workload": "2-D mesh [M=2,N=4] MLP (Decomp Fig. 3), bf16, B=8192 F=8192 H=32768: AG X "
                                    "along x, looped AG-einsum of W1 along y, AG W2 along y, looped einsum-RS along x",
                        "devices": m_x * n_y, "l2": "no flush: each step moves > 4 GB"}
@@ -506,7 +507,7 @@ class Mesh2D(Workload):
         from collective_fusedallreduce_gb300 import workloads
         if marks:
             marks[0].record(stream)
-        workloads.mlp_2d(self.x, self.w1, self.w2, self.mx, self.ny, self.bufs, stream)
+        workloads.mlp_2d(self.x, self.w1, self.w2, self.mx, self.ny, self.bufs, stream, self.side)
         if marks:
             marks[1].record(stream)
 

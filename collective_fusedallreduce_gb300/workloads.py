@@ -103,11 +103,17 @@ def mesh_order(blocks, m_x, n_y, group_axis):
     return [blocks[(x, y)] for x in range(m_x) for y in range(n_y)]
 
 
-def mlp_2d(x_blocks, w1_blocks, w2_blocks, m_x, n_y, bufs=None, stream=None):
+def mlp_2d(x_blocks, w1_blocks, w2_blocks, m_x, n_y, bufs=None, stream=None, side_stream=None):
     """Two-layer MLP on an [M, N] device mesh; device (x, y) holds
     X(x,y) = [B/N, F/M], W1(x,y) = [F/N, H/M], W2(x,y) = [H/M, F/N] (dicts
     keyed by (x, y)). Returns a dict of intermediate and output buffers keyed
     "xf", "h", "w2f", "y" (each a dict keyed by (x, y)).
+
+    With ``side_stream``, the AllGather of W2 (independent of the first einsum)
+    runs on it beside the first einsum, ordered by events: it starts once the
+    AllGather of X is done (so the einsum's persistent kernel is placed on the
+    SMs with it) and the Einsum-ReduceScatter waits for it. The results are the
+    same bits as the one-stream order.
     """
     keys = [(x, y) for x in range(m_x) for y in range(n_y)]
     bt, fm = x_blocks[(0, 0)].shape
@@ -121,18 +127,29 @@ def mlp_2d(x_blocks, w1_blocks, w2_blocks, m_x, n_y, bufs=None, stream=None):
             "w2f": {k: _empty((hm, f), dt, dev) for k in keys},
             "y": {k: _empty((bt, fm), dt, dev) for k in keys},
         }
+    main = stream if stream is not None else torch.cuda.current_stream(dev)
     # 1. AllGather X along x (subgroups of fixed y), on X's feature dimension
     coco.coco_allgather(coco.sliced(mesh_order(x_blocks, m_x, n_y, "y"), 1, ngroups=n_y),
-                        coco.replicated(mesh_order(bufs["xf"], m_x, n_y, "y"), ngroups=n_y), stream)
+                        coco.replicated(mesh_order(bufs["xf"], m_x, n_y, "y"), ngroups=n_y), main)
+    w2_stream = main
+    if side_stream is not None:
+        after_x = torch.cuda.Event()
+        after_x.record(main)  # also orders it after the previous call's reads of W2's gather
+        side_stream.wait_event(after_x)
+        w2_stream = side_stream
     # 2. Looped AllGather-Einsum of W1 along y (subgroups of fixed x), case 2 with the looped operand on the right
     coco.coco_looped_ag_einsum("mk,kn->mn", coco.local(mesh_order(bufs["xf"], m_x, n_y, "x"), ngroups=m_x),
                                coco.sliced(mesh_order(w1_blocks, m_x, n_y, "x"), 0, ngroups=m_x),
-                               coco.local(mesh_order(bufs["h"], m_x, n_y, "x"), ngroups=m_x), stream)
+                               coco.local(mesh_order(bufs["h"], m_x, n_y, "x"), ngroups=m_x), main)
     # 3. AllGather W2 along y (subgroups of fixed x), on W2's feature dimension
     coco.coco_allgather(coco.sliced(mesh_order(w2_blocks, m_x, n_y, "x"), 1, ngroups=m_x),
-                        coco.replicated(mesh_order(bufs["w2f"], m_x, n_y, "x"), ngroups=m_x), stream)
+                        coco.replicated(mesh_order(bufs["w2f"], m_x, n_y, "x"), ngroups=m_x), w2_stream)
+    if w2_stream is not main:
+        w2_done = torch.cuda.Event()
+        w2_done.record(w2_stream)
+        main.wait_event(w2_done)
     # 4. Looped Einsum-ReduceScatter along x (subgroups of fixed y) onto the feature dimension
     coco.coco_looped_einsum_rs("mk,kn->mn", coco.sliced(mesh_order(bufs["h"], m_x, n_y, "y"), 1, ngroups=n_y),
                                coco.sliced(mesh_order(bufs["w2f"], m_x, n_y, "y"), 0, ngroups=n_y),
-                               coco.sliced(mesh_order(bufs["y"], m_x, n_y, "y"), 1, ngroups=n_y), stream)
+                               coco.sliced(mesh_order(bufs["y"], m_x, n_y, "y"), 1, ngroups=n_y), main)
     return bufs

@@ -88,6 +88,28 @@ def test_megatron_tail_overlap_equals_the_unchunked_chain(coco, workloads, chunk
         assert torch.equal(out_a[q], out_b[q])
 
 
+def test_mesh_2d_mlp_side_stream_gives_the_same_bits(coco, workloads):
+    """The AllGather of W2 on a second stream beside the first einsum: the same outputs, bit for bit,
+    twice in a row (the second call's AllGather waits for the first call's reads of its buffer)."""
+    m_x, n_y = 2, 4
+    b, f, h = 64 * n_y, 64 * m_x * n_y, 128 * m_x
+    keys = [(x, y) for x in range(m_x) for y in range(n_y)]
+    xb = {k: synth.tensor(synth.seed_of(5, 3, i), (b // n_y, f // m_x), BF16).cuda() for i, k in enumerate(keys)}
+    w1 = {k: synth.tensor(synth.seed_of(5, 4, i), (f // n_y, h // m_x), BF16, std=f ** -0.5).cuda()
+          for i, k in enumerate(keys)}
+    w2 = {k: synth.tensor(synth.seed_of(5, 5, i), (h // m_x, f // n_y), BF16, std=h ** -0.5).cuda()
+          for i, k in enumerate(keys)}
+    one = workloads.mlp_2d(xb, w1, w2, m_x, n_y)
+    side = torch.cuda.Stream()
+    two = None
+    for _ in range(2):
+        two = workloads.mlp_2d(xb, w1, w2, m_x, n_y, two, side_stream=side)
+    coco.coco_device_status()
+    for name in ("xf", "h", "w2f", "y"):
+        for k in keys:
+            assert torch.equal(one[name][k], two[name][k]), (name, k)
+
+
 @pytest.mark.parametrize("m_x,n_y", [(2, 4), (1, 2), (2, 1)])
 def test_mesh_2d_mlp_small(coco, workloads, m_x, n_y):
     b, f, h = 64 * n_y, 64 * m_x * n_y, 128 * m_x
