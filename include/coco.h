@@ -27,7 +27,10 @@
  * ptr[g*nranks + r] is rank r of group g.
  *
  * Memory. Every pointer is a device pointer owned by the caller; each rank's
- * buffer is dense and row-major. The library allocates no device memory.
+ * buffer is dense and row-major. The library allocates no device memory; its
+ * own state is fixed-size device globals (an error word, and arrival counters
+ * for tensor-core launches whose CTAs wait on one another; up to 1024 such
+ * launches may be in flight at once).
  * Device pointers must be 16-byte aligned and the innermost per-rank
  * dimension a multiple of 8 elements, else COCO_ERR_ALIGN.
  *
