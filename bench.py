@@ -758,18 +758,33 @@ def aggregate_value(ideal_s, step_s, world):
 def measure_e2e(wl, stream, dev, dist, ideal, world, steps):
     """The step end to end through the public calls: every step uploads its inputs from pinned host
     memory and reads its result back, overlapping the compute of other steps; inputs and the result
-    are double-buffered, as a data loader would feed the step. The timed region spans the first
-    upload to the last read-back. Two arrangements are timed and the faster reported: uploads and
-    read-backs on one copy stream, or on two (concurrent directions); on GB300 the second wins for
-    small transfers and loses for multi-GB uploads, whose rate drops when read-backs run beside them."""
+    are double-buffered, as a data loader would feed the step. A loader packs a step's inputs into one
+    pinned staging buffer and the device tensors are views of one device buffer of the same layout, so
+    a step's upload is a single copy (one copy per tensor left gaps between the copies: 18 tensors on
+    the Megatron tail, 3128 on the BERT-large gradient list). The timed region spans the first upload
+    to the last read-back. Two arrangements are timed and the faster reported: uploads and read-backs
+    on one copy stream, or on two (concurrent directions)."""
     ins, result = wl.host_inputs()
     devs = [d for d, _ in ins]
     hosts = [h for _, h in ins]
     in_place = any(d is result for d in devs)
-    sets = [[d.data for d in devs], [torch.empty_like(d) for d in devs]]
+    originals = [d.data for d in devs]
+    result_original = result.data
+    align = 256  # every view starts on a 256-byte boundary, as an allocation would
+    sizes = [h.numel() * h.element_size() for h in hosts]
+    offs, total = [], 0
+    for n in sizes:
+        offs.append(total)
+        total += -(-n // align) * align
+    host_arena = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    for h, o, n in zip(hosts, offs, sizes):
+        host_arena[o:o + n].copy_(h.reshape(-1).view(torch.uint8))
+    del ins, hosts  # the staging buffer holds the inputs now
+    arenas = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+    sets = [[a[o:o + n].view(d.dtype).view(d.shape) for d, o, n in zip(devs, offs, sizes)] for a in arenas]
     outs = [result.data, None if in_place else torch.empty_like(result)]
     host_out = torch.empty(result.shape, dtype=result.dtype, pin_memory=True)
-    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    h2d = total
     d2h = host_out.numel() * host_out.element_size()
     up = torch.cuda.Stream(device=dev)
     down = up
@@ -782,14 +797,13 @@ def measure_e2e(wl, stream, dev, dist, ideal, world, steps):
             d.data = storage
         if not in_place:
             result.data = outs[b]
-        wl.rebind(b)
+        wl.rebind(("e2e", b))
 
     def upload(b, after_step):
         with torch.cuda.stream(up):
             if after_step:  # set b is free once its last step has computed (and, in place, been read back)
                 up.wait_event(downloaded[b] if in_place else computed[b])
-            for storage, h in zip(sets[b], hosts):
-                storage.copy_(h, non_blocking=True)
+            arenas[b].copy_(host_arena, non_blocking=True)
             uploaded[b].record(up)
 
     def run(n):
@@ -820,21 +834,26 @@ def measure_e2e(wl, stream, dev, dist, ideal, world, steps):
                 upload(b, True)
         e1.record(down)
         torch.cuda.synchronize()
-        bind(0)
         return e0.elapsed_time(e1) / 1000.0
 
     best = None
-    for mode in ("one copy stream", "two copy streams"):
-        down = up if mode == "one copy stream" else torch.cuda.Stream(device=dev)
-        run(2)
-        et = max_over_ranks(run(steps), dist, dev)
-        if best is None or et < best[0]:
-            best = (et, mode)
+    try:
+        for mode in ("one copy stream", "two copy streams"):
+            down = up if mode == "one copy stream" else torch.cuda.Stream(device=dev)
+            run(2)
+            et = max_over_ranks(run(steps), dist, dev)
+            if best is None or et < best[0]:
+                best = (et, mode)
+    finally:  # the workload's own tensors again (the staging buffers hold the same values)
+        for d, t in zip(devs, originals):
+            d.data = t
+        result.data = result_original
+        wl.rebind(0)
     et, mode = best
     return {"value": aggregate_value(ideal, et / steps, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": 1000.0 * et / steps,
-            "overlap": f"uploads and read-backs overlap the compute of other steps ({mode}); inputs and result "
-                       "double-buffered"}
+            "overlap": f"uploads and read-backs overlap the compute of other steps ({mode}); inputs packed in "
+                       "one pinned staging buffer, uploaded by one copy a step; inputs and result double-buffered"}
 
 
 # ------------------------------------------------------------------- main
