@@ -22,7 +22,7 @@ Sources, cited by title and section throughout:
   CollectiveEinsum (Alg. 1, Figs. 6 and 7) and its three AllGather cases.
 
 Every function states the passage it follows. Where the pages are silent the
-docstring says which reading was taken; all readings are listed in the design doc.
+docstring says which reading was taken and why.
 
 Pins: each public function is checked in ``tests/test_oracle_pins.py`` against
 facts the pages or mathematics fix (brute force, closed forms, identities the

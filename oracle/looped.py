@@ -8,7 +8,7 @@ shard whose ID travels with the data, an Update (DynamicUpdateSlice or
 Addition), and a CollectivePermute along the pairs {j -> j-1 mod N}.
 
 The page prints Alg. 1's caption but not its body. The body is reconstructed
-from the prose of §4 and §5.1 (the reading is listed in the design doc):
+from the prose of §4 and §5.1, read as follows:
 
 * AllGather: rank r starts with its own shard (shard IDs aligned with
   partition IDs at the loop start), computes, updates, and passes the shard to
@@ -173,8 +173,8 @@ def looped_einsum_reduce_scatter(spec, lhs_list, rhs_list, out_label, trace=None
 # Schedule variants of [Decomp] §5.4: loop unrolling by 2 (§5.4.1, Fig. 8) and
 # bidirectional data transfer (§5.4.2, Figs. 9 and 10). Both are presented as
 # optimisations that keep the loop semantically equivalent; the figures are not
-# printed, so the schedules below are restated from the prose (readings listed in
-# the design doc). Shard IDs travel with the data as in the ring forms above.
+# printed, so the schedules below are restated from the prose (a reading of it).
+# Shard IDs travel with the data as in the ring forms above.
 
 
 def _update(out, partial, update, o, sid, extent, n):
