@@ -299,7 +299,7 @@ COCO_EXPORT const char* coco_status_string(coco_status s) {
     case COCO_ERR_LAYOUT: return "COCO_ERR_LAYOUT: an operand has a layout the operation does not take";
     case COCO_ERR_ALIGN: return "COCO_ERR_ALIGN: pointer not 16-byte aligned or inner dim not a multiple of 8";
     case COCO_ERR_ALIAS: return "COCO_ERR_ALIAS: an output overlaps an input or another output";
-    case COCO_ERR_UNSUPPORTED: return "COCO_ERR_UNSUPPORTED: not implemented by this build";
+    case COCO_ERR_UNSUPPORTED: return "COCO_ERR_UNSUPPORTED: not implemented by this library";
     case COCO_ERR_CUDA: return "COCO_ERR_CUDA: a CUDA call or kernel launch failed";
     case COCO_ERR_TIMEOUT: return "COCO_ERR_TIMEOUT: a bounded device-side wait gave up";
     case COCO_ERR_VALUE: return "COCO_ERR_VALUE: a scalar argument is out of range";

@@ -69,7 +69,7 @@ typedef enum {
   COCO_ERR_LAYOUT = 4,      /* an operand has a layout the operation does not take */
   COCO_ERR_ALIGN = 5,       /* pointer not 16-byte aligned, or inner dim not a multiple of 8 */
   COCO_ERR_ALIAS = 6,       /* an output overlaps an input or another output */
-  COCO_ERR_UNSUPPORTED = 7, /* valid request outside what this build implements */
+  COCO_ERR_UNSUPPORTED = 7, /* valid request outside what this library implements */
   COCO_ERR_CUDA = 8,        /* a CUDA runtime call or kernel launch failed */
   COCO_ERR_TIMEOUT = 9,     /* a bounded device-side wait gave up */
   COCO_ERR_VALUE = 10       /* a scalar argument is out of range (e.g. dropout p) */
