@@ -579,6 +579,44 @@ class RsAg(Workload):
         return self.numel // 4096
 
 
+class AllReduceDirect(RsAg):
+    """The direct AllReduce of the same 1 GiB fp32 tensor over 8 ranks (one N-way reduction kernel,
+    no scratch), for comparison with the RS-AG split; bit-identical to it."""
+
+    name = "allreduce_direct"
+
+    def __init__(self, dev, n=8, numel=1 << 28, cfg=5, small=False):
+        super().__init__(dev, n, numel, cfg, small)
+        self.scratch = None
+        self.config = {"workload": f"AllReduce (direct N-way reduction), N=8 fp32, {self.numel} elements "
+                                   f"({self.numel * 4 >> 20} MiB) per rank, 8 distinct outputs", "ranks": n,
+                       "l2": f"no flush: each step moves {16 * self.numel * 4 >> 30} GiB"}
+
+    def kernels(self):
+        b = self.numel * 4
+        return [("k_fused_allreduce (no bias, residual or dropout)", "hbm", 2 * self.n * b, 1)]
+
+    def timed(self):
+        return self.kernels()
+
+    def step(self, stream, marks=None):
+        from collective_fusedallreduce_gb300 import coco
+        if marks:
+            marks[0].record(stream)
+        coco.coco_allreduce(coco.local(self.inp), coco.replicated(self.out), stream)
+        if marks:
+            marks[1].record(stream)
+
+    def oracle_sample(self, rows):
+        import oracle
+        from collective_fusedallreduce_gb300 import synth
+        cnt = rows * 4096
+        xs = [synth.as_f64(x[:cnt]) for x in self.inp]
+        t0 = time.perf_counter()
+        oracle.allreduce(xs)
+        return time.perf_counter() - t0, cnt / self.numel
+
+
 def bert_large_parameter_shapes(layers=24):
     """Parameter shapes of BERT-large (hidden 1024, 24 layers, FFN 4096, 30522-token vocabulary,
     512 positions): about 335 M elements, the size the scattered-tensor section quotes for BERT."""
@@ -660,7 +698,7 @@ class ScatteredGradients(Workload):
 
 
 WORKLOADS = {"c2": MegatronTail, "c2o": MegatronTailOverlap, "c2f": MegatronTailFused, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
-             "c5b": RsAg, "scatter": ScatteredGradients}
+             "c5b": RsAg, "c5d": AllReduceDirect, "scatter": ScatteredGradients}
 
 
 # --------------------------------------------------------------- helpers
@@ -928,7 +966,7 @@ def main():
         dist.barrier()
     from collective_fusedallreduce_gb300 import coco
 
-    wl = WORKLOADS[args.workload](dev, **({"small": True} if args.small and args.workload in ("c5b", "scatter") else {}))
+    wl = WORKLOADS[args.workload](dev, **({"small": True} if args.small and args.workload in ("c5b", "c5d", "scatter") else {}))
     stream = torch.cuda.current_stream(dev)
     kern = wl.timed()
     nk = len(kern)
