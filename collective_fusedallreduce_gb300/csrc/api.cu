@@ -554,6 +554,14 @@ COCO_EXPORT coco_status coco_scattered_table_build(int32_t ntensors, const int64
       }
     }
   }
+  // The upload reads a temporary host buffer: a stream capture would record a copy from memory
+  // freed on return, so a table is built outside capture.
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &capturing) != cudaSuccess ||
+      capturing != cudaStreamCaptureStatusNone) {
+    (void)cudaGetLastError();
+    return COCO_ERR_UNSUPPORTED;
+  }
   plan->table = table;
   plan->nbuckets = nb;
   plan->nranks = nranks;

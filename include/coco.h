@@ -40,6 +40,14 @@
  * `stream` and returns without synchronising. All N ranks of all groups are
  * processed by the one call.
  *
+ * CUDA graphs. Because no call synchronises or allocates, a sequence of calls
+ * may be captured into a CUDA graph (stream capture) and replayed; a replay
+ * repeats the launches with the pointers and sizes of the capture. A captured
+ * tensor-core launch whose CTAs wait on one another keeps the arrival counter
+ * it was given at capture (reset by a memset node before it), so two
+ * instantiations of one such graph must not run at the same time; launches of
+ * one instantiated graph are ordered behind each other by CUDA.
+ *
  * Aliasing. An output may not overlap any input, except where an entry point
  * says otherwise; violations return COCO_ERR_ALIAS.
  *
@@ -227,7 +235,9 @@ size_t coco_scattered_table_bytes(int32_t ntensors, const int64_t* numels, int32
  * `stream`) and fills `plan`. `tensors[r * ntensors + t]` is rank r's tensor t
  * (device pointer, 16-byte aligned, numels[t] elements of `dtype`, dense);
  * numels[t] < 2^32. Tensors may not overlap each other or the table
- * (COCO_ERR_ALIAS).
+ * (COCO_ERR_ALIAS). The upload reads a host buffer that lives only during the
+ * call, so a call on a stream under capture returns COCO_ERR_UNSUPPORTED (build
+ * the table first; the AllReduce itself may be captured).
  */
 coco_status coco_scattered_table_build(int32_t ntensors, const int64_t* numels, int32_t dtype, int32_t nranks,
                                        void* const* tensors, void* table, size_t table_bytes,
