@@ -58,18 +58,22 @@ constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 
 // its own 128-column half of B, 32 KB per stage, 6 stages. Four epilogue
 // warps (one per TMEM lane quarter) in both.
 //
-// The FusedAllReduce epilogue adds a third strip per epilogue warp, which the
-// residual tile is loaded into by TMA (one mbarrier per warp), and gives up
-// one or two stages for it.
+// The FusedAllReduce epilogue keeps the same depth of stages: each epilogue
+// warp has one output strip and one residual strip, which the next chunk's
+// residual is loaded into by TMA (one mbarrier per warp) while the current one
+// is computed. Its output strip is rewritten only once the previous chunk's
+// bulk stores (one per replica) have read it; its tiles have long K loops, so
+// the epilogue has the time, and the operand ring keeps its sixth stage
+// (2-3 % faster than two output strips and five stages).
 template <int MODE, bool TWO_SM>
 struct Cfg {
   static constexpr int B_STAGE = TWO_SM ? B_BYTES / 2 : B_BYTES;
   static constexpr int STAGE = A_BYTES + B_STAGE;
-  static constexpr int STAGES = MODE == 0 ? (TWO_SM ? 6 : 4) : (TWO_SM ? 5 : 3);
+  static constexpr int STAGES = TWO_SM ? 6 : 4;
   static constexpr int EPI_WARPS = 4;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int EPI_OFF = STAGES * STAGE;
-  static constexpr int STRIPS = MODE == 0 ? 2 : 3;  // two output strips (+ the residual strip)
+  static constexpr int STRIPS = 2;  // two output strips; FusedAllReduce: one output strip and the residual strip
   static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * STRIPS * EPI_STRIP;
   // full, empty, tmem full x2, tmem empty x2, drain (+ one residual barrier per epilogue warp)
   static constexpr int NUM_BARS = 2 * STAGES + 5 + (MODE == 0 ? 0 : EPI_WARPS);
@@ -203,6 +207,7 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // At most one committed bulk group may still be reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -692,7 +697,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
     // --------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
     const uint32_t strips = sbase + EPI_OFF + (warp - 2) * C::STRIPS * EPI_STRIP;
-    const uint32_t res_strip = strips + 2 * EPI_STRIP;  // fused mode only
+    const uint32_t res_strip = strips + EPI_STRIP;  // fused mode only
     const uint32_t res_bar = bar0 + 8u * (2 * STAGES + 5 + (warp - 2));
     uint32_t res_phase = 0;
     bool res_pending = false;
@@ -829,10 +834,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
             else mbar_arrive_relaxed(tempty_bar(acc));
           }
         }
-        // the strip about to be overwritten was handed to a bulk store two chunks ago
-        if (lane == 0) bulk_wait_read_le1();
+        // the strip about to be overwritten was handed to a bulk store two chunks ago (FusedAllReduce:
+        // its one output strip, to the stores of the previous chunk)
+        if (lane == 0) {
+          if constexpr (MODE == EPI_FUSED_ALLREDUCE) bulk_wait_read_all();
+          else bulk_wait_read_le1();
+        }
         __syncwarp();
-        const uint32_t strip = strips + buf * EPI_STRIP;
+        const uint32_t strip = MODE == EPI_FUSED_ALLREDUCE ? strips : strips + buf * EPI_STRIP;
 #pragma unroll
         for (int c = 0; c < 8; ++c)  // row = lane, 16-byte chunk c at its 128-byte-swizzle slot
           st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2],

@@ -150,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, 3) k_fused_allreduce(const __grid_co
   const char* bias = static_cast<const char*>(a.bias);
 
   const int64_t step = static_cast<int64_t>(gridDim.x) * kThreads * kUnroll;
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads * kUnroll + threadIdx.x; base < a.nvec;
-       base += step) {
+  // Blocks walk the vectors from the end: the partials a MatMul wrote last are still in L2 when this
+  // kernel follows it, and are read first.
+  for (int64_t base = static_cast<int64_t>(gridDim.x - 1 - blockIdx.x) * kThreads * kUnroll + threadIdx.x;
+       base < a.nvec; base += step) {
     float acc[kUnroll][VE];
     int64_t vi[kUnroll];
 #pragma unroll
