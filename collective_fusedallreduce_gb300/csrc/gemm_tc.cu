@@ -993,7 +993,9 @@ bool encode_out(CUtensorMap* map, const OutView& o, int dtype) {
   return r == CUDA_SUCCESS;
 }
 
-bool smem_configured[4][64] = {{false}};
+// per kernel variant and device: the dynamic shared-memory limit was raised (static storage: starts false;
+// atomic because calls may come from several host threads, which at worst both set the attribute)
+std::atomic<bool> smem_configured[4][64];
 
 }  // namespace
 
@@ -1049,10 +1051,10 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
   }
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !smem_configured[variant][dev]) {
+  if (dev >= 0 && dev < 64 && !smem_configured[variant][dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    smem_configured[variant][dev] = true;
+    smem_configured[variant][dev].store(true, std::memory_order_release);
   }
   // A-views are used with the A box and B-views with the B box; a view used
   // on both sides gets two maps.

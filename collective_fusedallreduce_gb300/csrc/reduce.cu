@@ -14,6 +14,7 @@
 // block per 256 vectors (many short blocks kept HBM busier than a few resident
 // blocks per SM) and stride over the data beyond 2^20 blocks.
 
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -461,15 +462,15 @@ cudaError_t rs_typed(const SliceArgs& a, int nranks, int ngroups, cudaStream_t s
 }  // namespace
 
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // per device, 0 until looked up (atomic: calls may come from several threads)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 cudaError_t launch_fused_allreduce(const FarLaunch& L, cudaStream_t s) {

@@ -40,6 +40,11 @@
  * `stream` and returns without synchronising. All N ranks of all groups are
  * processed by the one call.
  *
+ * Threads. Calls may come from several host threads at once: a call's host
+ * state is its own, the caches the library sets up once (kernel attributes,
+ * SM counts, device addresses) are atomic or locked, and
+ * coco_last_cuda_error() is per thread.
+ *
  * CUDA graphs. Because no call synchronises or allocates, a sequence of calls
  * may be captured into a CUDA graph (stream capture) and replayed; a replay
  * repeats the launches with the pointers and sizes of the capture. A captured
