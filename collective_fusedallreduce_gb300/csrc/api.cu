@@ -71,7 +71,11 @@ coco_status check_tensor(const coco_tensor* t, TInfo* o) {
     o->slice_dim = t->slice_dim;
     o->local[t->slice_dim] /= t->nranks;
   }
-  for (int d = 0; d < t->ndim; ++d) o->numel *= o->local[d];
+  // at most 2^40 elements per rank (far beyond any device's memory), so no size below overflows
+  for (int d = 0; d < t->ndim; ++d) {
+    if (o->local[d] != 0 && o->numel > (int64_t(1) << 40) / o->local[d]) return COCO_ERR_SHAPE;
+    o->numel *= o->local[d];
+  }
   o->bytes = o->numel * dtype_size(t->dtype);
   if (o->numel == 0) return COCO_OK;
   for (int i = 0; i < t->nranks * t->ngroups; ++i) {

@@ -104,6 +104,11 @@ def test_far_validation(coco):
     # residual
     assert far(coco, good_in, good_out, residual=mk(coco, F16, L, (4, 16), 2, base=FAKE + (1 << 42))) == 4
     assert far(coco, good_in, good_out, residual=mk(coco, F16, R, (8, 16), 2, base=FAKE + (1 << 42))) == 2
+    # more than 2^40 elements per rank is refused before any size is computed from it (no overflow)
+    huge = (1 << 40, 1 << 40, 16)
+    assert far(coco, mk(coco, F16, L, huge, 2), mk(coco, F16, R, huge, 2, base=FAKE + (1 << 40))) == 2
+    assert far(coco, mk(coco, F16, L, (1 << 20, 1 << 20, 16), 2),
+               mk(coco, F16, R, (1 << 20, 1 << 20, 16), 2, base=FAKE + (1 << 40))) == 2
 
 
 def test_far_at_index_base_validation(coco):
