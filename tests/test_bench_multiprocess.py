@@ -77,6 +77,38 @@ def test_roofline_peak_follows_the_power_regime():
     assert hbm["peak"] == 6000.0 and abs(hbm["frac"] - 0.5) < 1e-9
 
 
+def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed table while the kernel source still has the hash it was
+    captured at; a changed source, a missing source or an unknown key gives null."""
+    import hashlib
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_bytes(b"kernel v1")
+    digest = hashlib.sha256(b"kernel v1").hexdigest()[:16]
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text(
+        "# header line\n"
+        f"w:0 k.cu {digest} 12345\n"
+        "w:1 missing.cu 0000000000000000 7\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_traffic("w:0") == 12345
+    assert bench.load_traffic("w:1") is None
+    assert bench.load_traffic("w:2") is None
+    src.write_bytes(b"kernel v2")
+    assert bench.load_traffic("w:0") is None
+
+
+def test_committed_traffic_table_names_existing_sources():
+    """Every row of the committed table names a kernel source of this repository and a 16-hex digest."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    assert rows
+    for key, src, digest, byts in rows:
+        assert ":" in key and os.path.exists(os.path.join(ROOT, src)), (key, src)
+        assert len(digest) == 16 and int(digest, 16) >= 0 and int(byts) > 0
+
+
 def test_reference_arm_under_torchrun_two_ranks():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
