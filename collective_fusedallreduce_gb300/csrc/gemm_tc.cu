@@ -48,7 +48,6 @@ constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;             // 16 KB
 constexpr int B_BOX_BYTES = BK * 64 * 2;         // 8 KB (64 k-rows x 128 B)
 constexpr int B_BYTES = B_BOX_BYTES * (BN / 64);  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;    // 48 KB
 constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 B
 
 // Shared-memory budget. ONE CTA PER MMA (TWO_SM = false): each CTA of a pair
@@ -132,9 +131,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -238,9 +234,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "%5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 // Accumulator hand-back arrivals (own CTA / CTA 0 of the pair) with relaxed
 // semantics. Nothing in memory is published by them: the TMEM loads they
@@ -423,14 +416,6 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
-  return r;
-}
-
-__device__ __forceinline__ uint4 ld_nc_v4_hint(const void* p, uint64_t policy) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(policy));
   return r;
 }
 
