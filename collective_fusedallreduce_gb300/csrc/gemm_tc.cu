@@ -16,9 +16,10 @@
 //               boxes, 128B swizzle) into an mbarrier ring of stages.
 //   warp 1      allocates 512 TMEM columns (two fp32 128 x 256 accumulators)
 //               and issues tcgen05.mma from one elected lane: either one
-//               M=128, N=256 MMA per CTA, the pair sharing B by TMA multicast
-//               (4 stages of 48 KB), or, for long k-loops, one M=256 MMA over
-//               both CTAs (tcgen05 cta_group::2, 6 stages of 32 KB per CTA).
+//               M=128, N=256 MMA per CTA, each CTA loading its own A tile and
+//               the whole B tile (4 stages of 48 KB), or, for long k-loops, one
+//               M=256 MMA over both CTAs (tcgen05 cta_group::2, 6 stages of
+//               32 KB per CTA). No copy writes into another CTA's shared memory.
 //   warps 2..5  epilogue, one TMEM lane quarter each: tcgen05.ld 32 lanes x
 //               32 columns, convert (or, for the FusedAllReduce, add bias,
 //               apply dropout and add the residual), stage a 128-byte-wide
@@ -51,8 +52,8 @@ constexpr int B_BYTES = B_BOX_BYTES * (BN / 64);  // 32 KB
 constexpr int EPI_STRIP = 32 * 128;                 // one strip: 32 rows x 128 B
 
 // Shared-memory budget. ONE CTA PER MMA (TWO_SM = false): each CTA of a pair
-// receives the whole B tile (its own half plus the peer's, multicast), 48 KB
-// per stage, 4 stages. TWO_SM: the pair runs one M=256 MMA over both CTAs'
+// loads its A tile and the whole B tile into its own shared memory, 48 KB per
+// stage, 4 stages. TWO_SM: the pair runs one M=256 MMA over both CTAs'
 // shared memory (tcgen05 cta_group::2), each CTA holding its own A tile and
 // its own 128-column half of B, 32 KB per stage, 6 stages. Four epilogue
 // warps (one per TMEM lane quarter) in both.
@@ -209,16 +210,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// The same copy, written to the same shared-memory offset of every CTA in
-// `cta_mask` and completing the mbarrier at that offset in each of them.
-__device__ __forceinline__ void tma_load_3d_multicast(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
-                                                      int c1, int c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%4, "
-      "%5, %6}], [%2], %3;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "h"(cta_mask), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
 // The shared::cluster address of the same shared-memory offset in CTA 0 of the cluster.
 __device__ __forceinline__ uint32_t mapa_rank0(uint32_t addr) {
   uint32_t r;
@@ -310,13 +301,6 @@ __device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint64_t adesc, uint6
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
-// The same, arriving on the mbarrier at offset `bar` of every CTA in `cta_mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"(cta_mask)
       : "memory");
 }
@@ -471,8 +455,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA pair: both CTAs walk the same work units; CTA `rank` takes the unit's m-tile
-  // 2 * pair + rank, loads its own A tile and half of the shared B tile, and multicasts
-  // that half into both CTAs' shared memory.
+  // 2 * pair + rank. With one CTA per MMA each CTA loads its A tile and the whole B tile
+  // itself; with the pair MMA each loads its A tile and its 128 columns of B.
   const int rank = static_cast<int>(cluster_ctarank());
   const int cluster_id = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   constexpr uint16_t kPair = 0x3;
@@ -480,8 +464,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      // one CTA per MMA: freed when both CTAs' MMAs have read the stage; pair MMA: by CTA 0's commit
-      mbar_init(empty_bar(s), TWO_SM ? 1 : 2);
+      // freed by one commit: the CTA's own MMAs (one CTA per MMA) or CTA 0's pair MMAs
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -497,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
   }
   if (warp == 1) tmem_alloc<TWO_SM>(smem_u32(tmem_slot), TMEM_COLS);
   tc_fence_before();
-  cluster_sync();  // the peer's barriers exist before anything is multicast into them
+  cluster_sync();  // the peer's barriers exist before the pair MMA's copies or commits reach them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -582,12 +566,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
                   tma_load_3d_pair(sb + j * B_BOX_BYTES, mb, fb, bcol + rank * (BN / 2) + 64 * j, S.b_k0 + kb * BK,
                                    bb);
               } else {
-                mbar_expect_tx(full_bar(stage), STAGE_BYTES);  // own A + both halves of B
+                mbar_expect_tx(full_bar(stage), STAGE_BYTES);  // own A + the whole B tile
                 tma_load_3d(sa, ma, full_bar(stage), S.a_k0 + kb * BK, arow, ab);
 #pragma unroll
-                for (int j = rank * (BN / 128); j < (rank + 1) * (BN / 128); ++j)  // this CTA's half of B
-                  tma_load_3d_multicast(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb,
-                                        kPair);
+                for (int j = 0; j < BN / 64; ++j)
+                  tma_load_3d(sb + j * B_BOX_BYTES, mb, full_bar(stage), bcol + 64 * j, S.b_k0 + kb * BK, bb);
               }
             }
             if constexpr (TWO_SM) __syncwarp();
@@ -653,9 +636,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
               if constexpr (TWO_SM) umma_pair(d, ad + 2 * k, bd + 128 * k, idesc, accumulate);
               else umma(d, ad + 2 * k, bd + 128 * k, idesc, accumulate);
             }
-            // both producers may refill this stage
+            // the stage may be refilled (pair MMA: by both CTAs' producers)
             if constexpr (TWO_SM) umma_commit_pair(empty_bar(stage), kPair);
-            else umma_commit_multicast(empty_bar(stage), kPair);
+            else umma_commit(empty_bar(stage));
           }
           __syncwarp();
           any_mma = true;
@@ -879,7 +862,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA leaves while its peer may still multicast or commit into it
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers or read its TMEM
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
