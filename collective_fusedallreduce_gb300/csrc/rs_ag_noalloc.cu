@@ -23,9 +23,16 @@
 //     the AllGather reads it.
 //
 // Set-up: the first call on each device (with that device current) resolves
-// the device address of the array with cudaGetSymbolAddress and caches it;
-// later calls on that device reuse the address. Make that first call before
-// any stream capture.
+// the device address of the array with cudaGetSymbolAddress and caches it,
+// together with the identity of the CUDA context it belongs to; later calls in
+// the same context reuse the address. A new context on the device (after
+// cudaDeviceReset, for example) gets the array at a new address, so a call that
+// finds a different context resolves it again. Make the first call on a device
+// (and the first after a reset) before any stream capture: a call that needs
+// the set-up while its stream is being captured returns COCO_ERR_UNSUPPORTED
+// and launches nothing.
+
+#include <cuda.h>
 
 #include <mutex>
 
@@ -45,27 +52,78 @@ static __device__ __align__(256) unsigned char g_rs_ag_scratch[kNoAllocScratchBy
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+  unsigned long long ctx_id;  // the context the address belongs to (0: none cached)
+  void* addr;
+};
+ScratchSlot g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (set up once).
-cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_addr[dev]) {
+// Unique id of the calling thread's current CUDA context (driver entry points
+// looked up once through the runtime), or 0 when there is none or the driver
+// cannot tell.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_rs_ag_scratch);
-    if (e != cudaSuccess) return e;
-    if (!p) return cudaErrorInvalidSymbol;
-    g_scratch_addr[dev] = p;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+enum SetupResult { kSetupOk, kSetupUnderCapture, kSetupCudaError };
+
+// Device address of the scratch array in the current context of the current
+// device, resolved once per context. The resolution is refused while
+// `stream` is being captured.
+SetupResult scratch_address(cudaStream_t stream, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kSetupCudaError;
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  const unsigned long long ctx = current_context_id();
+  if (g_scratch[dev].addr && ctx != 0 && g_scratch[dev].ctx_id == ctx) {
+    *out = g_scratch[dev].addr;
+    return kSetupOk;
   }
-  *out = g_scratch_addr[dev];
-  return cudaSuccess;
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capturing) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return kSetupCudaError;
+  }
+  if (capturing != cudaStreamCaptureStatusNone) return kSetupUnderCapture;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_rs_ag_scratch) != cudaSuccess || !p) {
+    (void)cudaGetLastError();
+    return kSetupCudaError;
+  }
+  // the context exists now (the lookup initialises it); an unknown id caches nothing
+  g_scratch[dev].ctx_id = current_context_id();
+  g_scratch[dev].addr = g_scratch[dev].ctx_id ? p : nullptr;
+  *out = p;
+  return kSetupOk;
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// The extent rule of the library's other entry points: every dimension and
+// the per-rank element count at most 2^40, checked before any product can
+// overflow.
+constexpr int64_t kMaxElems = int64_t(1) << 40;
 
 }  // namespace
 
@@ -80,7 +138,8 @@ COCO_EXPORT coco_status coco_allreduce_rs_ag_noalloc(const coco_tensor* in, cons
   if (out->nranks != in->nranks || out->ngroups != in->ngroups) return COCO_ERR_SHAPE;
   int64_t numel = 1;
   for (int d = 0; d < in->ndim; ++d) {
-    if (in->shape[d] < 0 || in->shape[d] != out->shape[d]) return COCO_ERR_SHAPE;
+    if (in->shape[d] < 0 || in->shape[d] > kMaxElems || in->shape[d] != out->shape[d]) return COCO_ERR_SHAPE;
+    if (in->shape[d] != 0 && numel > kMaxElems / in->shape[d]) return COCO_ERR_SHAPE;
     numel *= in->shape[d];
   }
   if (in->shape[0] % in->nranks) return COCO_ERR_SHAPE;  // the scratch splits dimension 0
@@ -91,8 +150,11 @@ COCO_EXPORT coco_status coco_allreduce_rs_ag_noalloc(const coco_tensor* in, cons
   if (need > kNoAllocScratchBytes) return COCO_ERR_UNSUPPORTED;
 
   void* base = nullptr;
-  cudaError_t e = scratch_address(&base);
-  if (e != cudaSuccess) return COCO_ERR_CUDA;
+  switch (scratch_address(static_cast<cudaStream_t>(stream), &base)) {
+    case kSetupOk: break;
+    case kSetupUnderCapture: return COCO_ERR_UNSUPPORTED;
+    default: return COCO_ERR_CUDA;
+  }
 
   // The scratch as a caller would have passed it: SLICED on dimension 0, one
   // 256-byte-aligned slice per (group, rank).

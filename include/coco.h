@@ -195,9 +195,15 @@ coco_status coco_allreduce_rs_ag(const coco_tensor* in, const coco_tensor* scrat
  *   - A call needs ngroups * numel * element-size bytes (plus per-slice
  *     rounding to 256 bytes); larger requests return COCO_ERR_UNSUPPORTED
  *     before any CUDA call.
+ *   - Extents follow the library's usual rule (each dimension and the
+ *     per-rank element count at most 2^40, else COCO_ERR_SHAPE), checked
+ *     before any size is multiplied.
  *   - The first call on a device (with that device current) looks up the
- *     array's device address with cudaGetSymbolAddress and caches it; make
- *     that first call before any stream capture.
+ *     array's device address with cudaGetSymbolAddress and caches it for the
+ *     current CUDA context; a call in a new context (after cudaDeviceReset,
+ *     say) looks it up again. Make the first call in a context before any
+ *     stream capture: a call that needs the look-up while `stream` is being
+ *     captured returns COCO_ERR_UNSUPPORTED and launches nothing.
  *   - All calls share the array and it keeps the last call's contents
  *     (nothing needs to start at zero: the ReduceScatter writes every element
  *     the AllGather reads). Calls whose kernels can overlap on the GPU race on

@@ -270,3 +270,24 @@ def test_scattered_table_validation(coco):
     assert lib.coco_scattered_allreduce(ctypes.byref(p2), ctypes.c_float(1.0), None) == 0  # nothing to do
     p3 = coco.CocoScatteredPlan(None, 5, 2, coco.F16)
     assert lib.coco_scattered_allreduce(ctypes.byref(p3), ctypes.c_float(1.0), None) == 1
+
+
+def test_noalloc_rejects_overflowing_extents_before_any_cuda_call(coco):
+    """Extents are range-checked one by one before they are multiplied: a shape whose product
+    overflows 64 bits is refused with COCO_ERR_SHAPE like the caller-scratch entry point refuses it,
+    not wrapped to an empty tensor."""
+    F32, L, R, S = coco.F32, coco.LOCAL, coco.REPLICATED, coco.SLICED
+    n = 8
+    huge = (1 << 22, 1 << 21, 1 << 21)  # 2^64 elements: wraps to 0 in a plain int64 product
+    for shape in [huge, (8, (1 << 40) + 8), (1 << 21, 1 << 20, 8)]:
+        t = mk(coco, F32, L, shape, n)
+        o = mk(coco, F32, R, shape, n, base=FAKE + (1 << 40))
+        assert coco.raw_call("coco_allreduce_rs_ag_noalloc", ctypes.byref(t), ctypes.byref(o), None) == 2, shape
+        sc = mk(coco, F32, S, shape, n, slice_dim=0, base=FAKE + (2 << 40))
+        assert coco.raw_call("coco_allreduce_rs_ag", ctypes.byref(t), ctypes.byref(sc), ctypes.byref(o),
+                             None) == 2, shape
+    # structural errors still come first and an empty tensor is still a no-op
+    t = mk(coco, F32, L, (0, 16), n)
+    o = mk(coco, F32, R, (0, 16), n, base=FAKE + (1 << 40))
+    assert coco.raw_call("coco_allreduce_rs_ag_noalloc", ctypes.byref(t), ctypes.byref(o), None) == 0
+    assert coco.raw_call("coco_allreduce_rs_ag_noalloc", None, ctypes.byref(o), None) == 1
