@@ -2,19 +2,27 @@
 """Benchmark of the fused / looped collectives on one GB300 (or N replicas).
 
 A step is one pass of the hot path over one batch of synthetic input, all N
-logical ranks on this GPU. The default workload is the Megatron self-attention
-output projection of [CoCoNet] Fig. 3: 8 ranks, fp16, in[8,1024,4096] sliced
-on its last dimension, w[4096,4096] sliced on its first, the local MatMul per
-rank, then FusedAllReduce with bias[4096], dropout p=0.1 and a replicated
-residual[8,1024,4096]. ``--workload`` selects the other workloads (looped
-einsum cases, the 2-D mesh MLP, RS-AG), each printed as its own line.
+logical ranks on this GPU. The default (headline) workload is the Megatron
+self-attention output projection of [CoCoNet] Fig. 3: 8 ranks, fp16,
+in[8,1024,4096] sliced on its last dimension, w[4096,4096] sliced on its
+first, bias[4096], dropout p=0.1 and a replicated residual[8,1024,4096], with
+the per-rank MatMul fused into the FusedAllReduce (one tensor-core kernel; no
+partial is stored). After it, in the same process, every other configuration
+is timed and reported as a sub-record under ``configs``: the unfused chain of
+the same tail (``c2``: local MatMul, then FusedAllReduce), the looped
+AllGather-Einsum cases 1/2/3 (``c3``, ``c4a``, ``c4b``), the 2-D mesh MLP
+(``c5``), the RS-AG split AllReduce and the direct AllReduce of 1 GiB fp32 x 8
+(``c5b``, ``c5d``) and the scattered-tensor AllReduce (``scatter``).
+``--workload`` selects another headline (then no sub-records unless
+``--configs`` names them).
 
 ``value`` is the step's throughput as a percentage of one GB300's roofline:
-100 * (sum over the step's kernels of algorithmic work / measured peak) /
-measured step time, with the peaks of MEASURED_PEAKS.json (HBM copy GB/s and
-cuBLAS bf16 TFLOP/s; fp16 runs at the bf16 rate). Under torchrun every rank
-runs an independent replica on its own GPU (weak scaling) and ``value`` sums
-the replicas' throughput.
+100 * ideal step time / measured step time, the ideal being the workload's own
+roofline at the peaks of MEASURED_PEAKS.json (HBM copy GB/s and cuBLAS bf16
+TFLOP/s burst; fp16 runs at the bf16 rate): for the fused tail max(MatMul
+FLOPs, minimal traffic), for a chain of kernels the sum of each kernel's
+ideal. Under torchrun every rank runs an independent replica on its own GPU
+(weak scaling) and ``value`` sums the replicas' throughput.
 
 ``--impl reference`` times the CPU oracle (plain float64 NumPy) on host cores
 on a bounded sample of the same workload, in the same unit.
@@ -729,11 +737,11 @@ def cpu_oracle_rate(wl, peaks, budget_s, min_rows=1):
     return value, dt, rows, frac
 
 
-def roofline_entry(name, bound, units, avg_s, peaks, traffic, power_capped=False):
-    """A tensor-bound kernel that ran under the power cap (sw_power_cap seen during the timed
-    region) is held to the sustained bf16 figure, which was measured in that same regime (a
-    seconds-long GEMM loop at the power cap); otherwise to the burst figure. The fraction of the
-    burst figure is reported beside it either way."""
+def roofline_entry(name, bound, units, avg_s, peaks, traffic, clk=None):
+    """The roofline of one timed segment. Tensor-bound kernels are rated against the burst bf16
+    figure (a kernel timed by itself, for milliseconds at most); HBM-bound ones against the copy
+    figure. When the clock record shows the power cap holding the SM clock down during the timed
+    region, the fraction of the sustained bf16 figure (measured in that regime) is added as a note."""
     src = "MEASURED_PEAKS.json" if peaks["source"] == "measured" else "fallback"
     extra = {}
     if bound == "hbm":
@@ -744,15 +752,22 @@ def roofline_entry(name, bound, units, avg_s, peaks, traffic, power_capped=False
     else:
         achieved = units / avg_s / 1e12
         unit = "TFLOP/s"
-        if power_capped:
-            peak = peaks["bf16_tflops_sustained"]
-            src += " (sustained: sw_power_cap during the timed region)"
-            extra["frac_of_burst"] = round(achieved / peaks["bf16_tflops"], 4)
-        else:
-            peak = peaks["bf16_tflops"]
-            src += " (burst)"
+        peak = peaks["bf16_tflops"]
+        src += " (burst)"
+        extra["frac_of_burst"] = round(achieved / peak, 4)
+        if clk and power_capped_low(clk):
+            extra["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+            extra["note"] = (f"sw_power_cap active, median SM clock {clk['sm_mhz']:.0f} of "
+                             f"{clk['sm_max_mhz']:.0f} MHz: frac_of_sustained is the fraction of the "
+                             f"power-capped bf16 figure")
     return dict({"kernel": name, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
                  "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": src}, **extra)
+
+
+def power_capped_low(clk):
+    """The power cap was active and held the median SM clock at least 3 % below its maximum."""
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    return "sw_power_cap" in (clk.get("reasons") or []) and bool(sm) and bool(mx) and sm < 0.97 * mx
 
 
 def load_traffic(kernel_key):
@@ -928,13 +943,108 @@ def run_reference(args, peaks):
     return 0
 
 
+def time_steps(wl, stream, dev, dist, steps, warmup, local_rank):
+    """Warm-up, then exactly ``steps`` steps timed with CUDA events on the launching stream, bracketed
+    by a barrier and a device synchronisation on both sides; clocks sampled meanwhile. Returns the
+    slowest rank's step time, the per-segment times (events between a step's calls), the clock
+    record and the number of the library's kernel launches in the timed region."""
+    from collective_fusedallreduce_gb300 import coco
+    kern = wl.timed()
+    nk = len(kern)
+    for _ in range(warmup):
+        wl.step(stream)
+    coco.coco_device_status(stream)
+    torch.cuda.synchronize()
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = coco.coco_kernel_launches()
+    start.record(stream)
+    for k in range(steps):
+        wl.step(stream, marks[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    launches = coco.coco_kernel_launches() - launches0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    coco.coco_device_status(stream)  # raises if a bounded device wait gave up
+    elapsed = max_over_ranks(start.elapsed_time(end) / 1000.0, dist, dev)
+    per_kernel = [sum(marks[k][i].elapsed_time(marks[k][i + 1]) for k in range(steps)) / 1000.0 / steps
+                  for i in range(nk)]
+    return elapsed / steps, per_kernel, clk, int(launches)
+
+
+def rooflines(key, wl, per_kernel, peaks, clk):
+    """(dominant segment's roofline entry, per-segment breakdown)."""
+    kern = wl.timed()
+    i_dom = int(np.argmax(per_kernel))
+    name, bound, units, _ = kern[i_dom]
+    roof = roofline_entry(name, bound, units, per_kernel[i_dom], peaks, load_traffic(f"{key}:{i_dom}"), clk)
+    breakdown = []
+    for i, (name, bound, units, _) in enumerate(kern):
+        e = roofline_entry(name, bound, units, per_kernel[i], peaks, None, clk)
+        breakdown.append({"kernel": name, "bound": bound, "us": round(per_kernel[i] * 1e6, 1),
+                          "achieved": e["achieved"], "unit": e["unit"], "frac": e["frac"]})
+    if hasattr(wl, "flops"):  # an HBM-bound contraction: its tensor-pipe rate beside it
+        roof["tensor_tflops"] = round(wl.flops() / per_kernel[i_dom] / 1e12, 1)
+        roof["tensor_frac_of_burst"] = round(wl.flops() / per_kernel[i_dom] / 1e12 / peaks["bf16_tflops"], 4)
+    return roof, breakdown
+
+
+# Every configuration besides the headline, each timed in the same process after it (one GPU's
+# memory at a time: the previous workload's tensors are freed first).
+SUB_CONFIGS = ["c2", "c3", "c4a", "c4b", "c5", "c5b", "c5d", "scatter"]
+
+
+def sub_record(key, dev, dist, world, peaks, args, local_rank):
+    """One configuration's measurement for the ``configs`` map of the bench line. The step count is
+    at least ``--steps`` and enough for about ``--sub-seconds`` of timed work, so that the clock
+    record holds samples from under load."""
+    wl = WORKLOADS[key](dev)
+    stream = torch.cuda.current_stream(dev)
+    warm = max(3, args.warmup)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(warm):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    est = (time.perf_counter() - t0) / warm
+    est = max_over_ranks(est, dist, dev)
+    steps = int(max(args.steps, min(5000, args.sub_seconds / max(est, 1e-6))))
+    step_s, per_kernel, clk, launches = time_steps(wl, stream, dev, dist, steps, 3, local_rank)
+    roof, breakdown = rooflines(key, wl, per_kernel, peaks, clk)
+    ideal = wl.ideal_seconds(peaks)
+    rec = {"workload": wl.config["workload"], "dtype": wl.dtype, "steps": steps, "ms_per_step": step_s * 1e3,
+           "ideal_ms_per_step": ideal * 1e3, "value": aggregate_value(ideal, step_s, world), "unit": UNIT,
+           "kernel": roof["kernel"], "bound": roof["bound"], "achieved": roof["achieved"], "unit_achieved":
+           roof["unit"], "frac": roof["frac"], "traffic": roof["traffic"], "roofline": roof, "kernels": breakdown,
+           "clocks": clk, "gpu_launches": launches}
+    if "frac_of_burst" in roof:
+        rec["frac_of_burst"] = roof["frac_of_burst"]
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="coco", choices=["coco", "reference"])
-    ap.add_argument("--workload", default="c2", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="c2f", choices=sorted(WORKLOADS))
+    ap.add_argument("--configs", default=None,
+                    help="comma-separated configurations timed after the headline workload, each a sub-record "
+                         "of the line (default: every other configuration when the headline is the default "
+                         "workload; 'none' for none)")
+    ap.add_argument("--sub-seconds", type=float, default=0.25,
+                    help="timed work per sub-record, at least --steps steps")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -964,63 +1074,30 @@ def main():
         __graft_entry__.build()
     if dist is not None:
         dist.barrier()
-    from collective_fusedallreduce_gb300 import coco
+
+    if args.configs is None:
+        subs = [c for c in SUB_CONFIGS if c != args.workload] if args.workload == "c2f" else []
+    elif args.configs == "none":
+        subs = []
+    else:
+        subs = [c for c in args.configs.split(",") if c]
+        for c in subs:
+            if c not in WORKLOADS:
+                raise SystemExit(f"unknown configuration {c!r}")
 
     wl = WORKLOADS[args.workload](dev, **({"small": True} if args.small and args.workload in ("c5b", "c5d", "scatter") else {}))
     stream = torch.cuda.current_stream(dev)
-    kern = wl.timed()
-    nk = len(kern)
-
-    for _ in range(args.warmup):
-        wl.step(stream)
-    coco.coco_device_status(stream)
-    torch.cuda.synchronize()
-
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    launches0 = coco.coco_kernel_launches()
-    start.record(stream)
-    for k in range(args.steps):
-        wl.step(stream, marks[k])
-    end.record(stream)
-    torch.cuda.synchronize()
-    launches = coco.coco_kernel_launches() - launches0
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop()
-    coco.coco_device_status(stream)
-    elapsed = start.elapsed_time(end) / 1000.0
-    per_kernel = [sum(marks[k][i].elapsed_time(marks[k][i + 1]) for k in range(args.steps)) / 1000.0 / args.steps
-                  for i in range(nk)]
-    elapsed = max_over_ranks(elapsed, dist, dev)
-
-    step_s = elapsed / args.steps
+    step_s, per_kernel, clk, launches = time_steps(wl, stream, dev, dist, args.steps, args.warmup, local_rank)
     ideal = wl.ideal_seconds(peaks)
     value = aggregate_value(ideal, step_s, world)
-
-    # dominant timed segment's roofline, timed with events on the launching stream
-    i_dom = int(np.argmax(per_kernel))
-    name, bound, units, _ = kern[i_dom]
-    capped = "sw_power_cap" in (clk.get("reasons") or [])
-    roof = roofline_entry(name, bound, units, per_kernel[i_dom], peaks, load_traffic(f"{args.workload}:{i_dom}"),
-                          capped)
-    breakdown = []
-    for i, (name, bound, units, _) in enumerate(kern):
-        e = roofline_entry(name, bound, units, per_kernel[i], peaks, None, capped)
-        breakdown.append({"kernel": name, "us": round(per_kernel[i] * 1e6, 1), "achieved": e["achieved"],
-                          "unit": e["unit"], "frac": e["frac"]})
+    roof, breakdown = rooflines(args.workload, wl, per_kernel, peaks, clk)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_s * 1000.0, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded torch CUDA generator)",
             "config": dict(wl.config, parallelism=f"{wl.config.get('ranks', 8)} logical ranks in one GPU"
                            + (f" x {world} replicas" if world > 1 else "")),
-            "roofline": roof, "kernels": breakdown, "gpu_launches": int(launches), "clocks": clk,
+            "roofline": roof, "kernels": breakdown, "gpu_launches": launches, "clocks": clk,
             "ideal_ms_per_step": ideal * 1000.0}
 
     # end to end: host buffers in, result back, through the same public calls
@@ -1032,6 +1109,11 @@ def main():
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": host_threads(), "kind": "oracle",
                                 "sample": f"{rows} of {wl.full_sample()} {wl.sample_unit()} of every rank, one pass, "
                                           f"{dt:.2f} s (fraction {frac:.3g} of one step)"}
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if subs:
+        line["configs"] = {c: sub_record(c, dev, dist, world, peaks, args, local_rank) for c in subs}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:

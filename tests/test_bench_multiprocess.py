@@ -62,19 +62,25 @@ def test_single_process_helpers_without_a_process_group():
     assert abs(bench.aggregate_value(1.0, 2.0, 1) - 50.0) < 1e-12
 
 
-def test_roofline_peak_follows_the_power_regime():
-    """Tensor-bound kernels are held to the burst bf16 figure, or to the sustained one when the
-    clock record saw sw_power_cap; HBM-bound kernels always to the copy figure."""
+def test_roofline_is_rated_against_the_burst_peak():
+    """Tensor-bound kernels are rated against the burst bf16 figure whatever the clock record says;
+    when the power cap held the median clock down, the fraction of the sustained figure is added as a
+    note. HBM-bound kernels are always rated against the copy figure."""
     sys.path.insert(0, ROOT)
     import bench
     peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "source": "measured"}
-    burst = bench.roofline_entry("k", "tensor", 1.6e12, 1e-3, peaks, None, False)
-    assert burst["peak"] == 2000.0 and abs(burst["frac"] - 0.8) < 1e-9 and "frac_of_burst" not in burst
-    capped = bench.roofline_entry("k", "tensor", 1.6e12, 1e-3, peaks, 123, True)
-    assert capped["peak"] == 1600.0 and abs(capped["frac"] - 1.0) < 1e-9
-    assert abs(capped["frac_of_burst"] - 0.8) < 1e-9 and capped["traffic"] == 123
-    hbm = bench.roofline_entry("k", "hbm", 3e9, 1e-3, peaks, None, True)
-    assert hbm["peak"] == 6000.0 and abs(hbm["frac"] - 0.5) < 1e-9
+    burst = bench.roofline_entry("k", "tensor", 1.6e12, 1e-3, peaks, None)
+    assert burst["peak"] == 2000.0 and abs(burst["frac"] - 0.8) < 1e-9
+    assert abs(burst["frac_of_burst"] - 0.8) < 1e-9 and "frac_of_sustained" not in burst
+    capped_clk = {"sm_mhz": 1400.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    capped = bench.roofline_entry("k", "tensor", 1.6e12, 1e-3, peaks, 123, capped_clk)
+    assert capped["peak"] == 2000.0 and abs(capped["frac"] - 0.8) < 1e-9 and capped["traffic"] == 123
+    assert abs(capped["frac_of_sustained"] - 1.0) < 1e-9 and "note" in capped
+    # the cap flagged but the clock at its maximum: no sustained note
+    full_clk = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    assert "frac_of_sustained" not in bench.roofline_entry("k", "tensor", 1.6e12, 1e-3, peaks, None, full_clk)
+    hbm = bench.roofline_entry("k", "hbm", 3e9, 1e-3, peaks, None, capped_clk)
+    assert hbm["peak"] == 6000.0 and abs(hbm["frac"] - 0.5) < 1e-9 and "frac_of_burst" not in hbm
 
 
 def test_traffic_is_reported_only_for_the_captured_source(tmp_path, monkeypatch):
