@@ -19,7 +19,8 @@ Sources, cited by title and section throughout:
   in Large Deep Learning Models" (ASPLOS '23; the page is a set of notes on the
   paper): §2.1 collective definitions, §2.2 the 1-D / 2-D partitioned MLPs of
   Figs. 2 and 3, §4 the decomposition idea (Figs. 4 and 5), §5.1 the Looped
-  CollectiveEinsum (Alg. 1, Figs. 6 and 7) and its three AllGather cases.
+  CollectiveEinsum (Alg. 1, Figs. 6 and 7) and its three AllGather cases,
+  §5.5 the cost model that enables it.
 
 Every function states the passage it follows. Where the pages are silent the
 docstring says which reading was taken and why.
@@ -61,6 +62,7 @@ from .scattered import (
     scattered_allreduce,
     scattered_allreduce_by_buckets,
 )
+from .costmodel import loop_profitable
 from .mlp import (
     mlp_1d_forward,
     mlp_1d_reference,
@@ -81,4 +83,5 @@ __all__ = [
     "mlp_1d_forward", "mlp_1d_reference", "mlp_2d_forward", "mlp_2d_reference",
     "megatron_attention_tail",
     "scattered_buckets", "scattered_metadata_bytes", "scattered_allreduce", "scattered_allreduce_by_buckets",
+    "loop_profitable",
 ]

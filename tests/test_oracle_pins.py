@@ -543,3 +543,56 @@ def test_scattered_allreduce_closed_form_and_bucket_walk(n):
     b = oracle.scattered_allreduce_by_buckets(rnd, 0.25)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+# ---------------------------------------------------------------- [Decomp] §5.5 cost model
+
+_TIMES = [0.0, 0.5, 1.0, 2.0, 3.0, 7.5]
+
+
+def test_cost_model_ring_no_slower_than_the_collective_always_pays():
+    # with ring_comm <= orig_comm and no prologue / epilogue, overlapping can only help:
+    # comp + comm >= max(comp, ring) whichever of comp and ring is larger
+    for comp in _TIMES:
+        for comm in _TIMES:
+            for ring in _TIMES:
+                if ring <= comm:
+                    assert oracle.loop_profitable(comp, comm, ring, 0.0)
+
+
+def test_cost_model_half_bandwidth_ring_closed_form():
+    # §5.5's concern: the ring uses one dimension of a mesh, half the bandwidth, so ring = 2 * comm.
+    # Then (no epilogue) the loop pays exactly when the computation is at least the original comm.
+    for comp in _TIMES:
+        for comm in _TIMES:
+            assert oracle.loop_profitable(comp, comm, 2.0 * comm, 0.0) == (comp >= comm)
+
+
+def test_cost_model_boundary_and_special_cases():
+    assert oracle.loop_profitable(4.0, 2.0, 5.0, 1.0)        # 6 >= max(4, 5) + 1: equality enables
+    assert not oracle.loop_profitable(4.0, 2.0, 5.0, 1.5)    # 6 <  6.5
+    assert oracle.loop_profitable(10.0, 4.0, 8.0, 1.0)       # 14 >= 11
+    assert not oracle.loop_profitable(2.0, 4.0, 8.0, 0.0)    # 6 < 8
+    # no communication at all: the loop pays only when its ring is free and it adds nothing
+    assert oracle.loop_profitable(3.0, 0.0, 0.0, 0.0)
+    assert not oracle.loop_profitable(3.0, 0.0, 0.0, 0.5)
+    assert not oracle.loop_profitable(3.0, 0.0, 3.5, 0.0)
+    # compute-dominated: the ring is hidden, the saving is the original comm minus the epilogue
+    assert oracle.loop_profitable(100.0, 5.0, 20.0, 5.0)
+    assert not oracle.loop_profitable(100.0, 5.0, 20.0, 5.01)
+    with pytest.raises(ValueError):
+        oracle.loop_profitable(-1.0, 0.0, 0.0, 0.0)
+    with pytest.raises(ValueError):
+        oracle.loop_profitable(1.0, float("nan"), 0.0, 0.0)
+
+
+def test_cost_model_epilogue_is_monotone():
+    # a dearer prologue / epilogue can only switch the decision from "decompose" to "keep"
+    for comp in _TIMES:
+        for comm in _TIMES:
+            for ring in _TIMES:
+                seen_false = False
+                for e in _TIMES:
+                    d = oracle.loop_profitable(comp, comm, ring, e)
+                    assert not (seen_false and d)
+                    seen_false = seen_false or not d
