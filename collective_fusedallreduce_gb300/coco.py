@@ -105,6 +105,12 @@ _lib.coco_status_string.restype = ctypes.c_char_p
 _lib.coco_last_cuda_error.restype = ctypes.c_int
 _lib.coco_version.restype = ctypes.c_int
 _lib.coco_kernel_launches.restype = ctypes.c_uint64
+_lib.coco_shard_order.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.POINTER(ctypes.c_int32)]
+_lib.coco_shard_order.restype = ctypes.c_int
+_lib.coco_loop_profitable.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                                      ctypes.POINTER(ctypes.c_int32)]
+_lib.coco_loop_profitable.restype = ctypes.c_int
 
 EXPORTED = [
     "coco_fused_allreduce", "coco_fused_allreduce_at", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
@@ -113,6 +119,7 @@ EXPORTED = [
     "coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched", "coco_dropout_keep_mask",
     "coco_scattered_table_bytes", "coco_scattered_table_build", "coco_scattered_allreduce",
     "coco_device_status", "coco_wait_selftest", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
+    "coco_shard_order", "coco_loop_profitable",
 ]
 
 
@@ -305,3 +312,24 @@ def coco_scattered_table_build(per_rank, table, stream=None):
 
 def coco_scattered_allreduce(plan, alpha=1.0, stream=None):
     _check(_lib.coco_scattered_allreduce(ctypes.byref(plan), float(alpha), _stream(stream)), "coco_scattered_allreduce")
+
+
+AG_ORDER, RS_ORDER = 0, 1
+
+
+def coco_shard_order(kind, schedule, rank, nranks):
+    """The planner's shard schedule for one rank (see coco.h): kind AG_ORDER gives the shard visited at
+    each AllGather-Einsum step, RS_ORDER the rank whose partial output shard ``rank`` collects at each
+    Einsum-ReduceScatter step."""
+    arr = (ctypes.c_int32 * max(1, int(nranks)))()
+    _check(_lib.coco_shard_order(int(kind), int(schedule), int(rank), int(nranks), arr), "coco_shard_order")
+    return [int(arr[i]) for i in range(int(nranks))]
+
+
+def coco_loop_profitable(orig_comp, orig_comm, ring_comm, epilogue_cost):
+    """[Decomp] §5.5 cost model: True when the Looped CollectiveEinsum is expected to beat the original
+    collective followed by the einsum (times in one unit)."""
+    out = ctypes.c_int32(-1)
+    _check(_lib.coco_loop_profitable(float(orig_comp), float(orig_comm), float(ring_comm), float(epilogue_cost),
+                                     ctypes.byref(out)), "coco_loop_profitable")
+    return bool(out.value)

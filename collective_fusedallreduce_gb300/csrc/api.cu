@@ -963,3 +963,24 @@ COCO_EXPORT coco_status coco_looped_einsum_rs_sched(const char* spec, const coco
                                                     const coco_tensor* out, int schedule, void* stream) {
   return looped_einsum_rs(spec, lhs, rhs, out, schedule, stream);
 }
+
+COCO_EXPORT coco_status coco_shard_order(int32_t kind, int32_t schedule, int32_t rank, int32_t nranks,
+                                         int32_t* order) {
+  if (!order) return COCO_ERR_NULL;
+  if (nranks < 1 || nranks > COCO_MAX_PTRS || rank < 0 || rank >= nranks) return COCO_ERR_SHAPE;
+  if ((kind != 0 && kind != 1) || !valid_schedule(schedule)) return COCO_ERR_VALUE;
+  const std::vector<int> o = kind == 0 ? ag_order(rank, nranks, schedule) : rs_order(rank, nranks, schedule);
+  for (int i = 0; i < nranks; ++i) order[i] = o[i];
+  return COCO_OK;
+}
+
+// [Decomp] §5.5: decompose only when
+//   orig_comp + orig_comm >= max(orig_comp, ring_comm) + epilogue_cost.
+COCO_EXPORT coco_status coco_loop_profitable(double orig_comp, double orig_comm, double ring_comm,
+                                             double epilogue_cost, int32_t* profitable) {
+  if (!profitable) return COCO_ERR_NULL;
+  for (double t : {orig_comp, orig_comm, ring_comm, epilogue_cost})
+    if (!std::isfinite(t) || t < 0.0) return COCO_ERR_VALUE;
+  *profitable = orig_comp + orig_comm >= std::max(orig_comp, ring_comm) + epilogue_cost ? 1 : 0;
+  return COCO_OK;
+}

@@ -371,6 +371,38 @@ coco_status coco_looped_ag_einsum_sched(const char* spec, const coco_tensor* lhs
 coco_status coco_looped_einsum_rs_sched(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
                                         const coco_tensor* out, int schedule, void* stream);
 
+/*
+ * The shard schedule the looped entry points follow, for callers that run the
+ * loop themselves (one rank per process, the permutes over a network):
+ *   kind 0 (AllGather-Einsum):  order[i] = the shard rank `rank` computes on at
+ *                               step i;
+ *   kind 1 (Einsum-ReduceScatter): order[i] = the rank whose partial output
+ *                               shard `rank` receives at step i (the fp32
+ *                               accumulation order).
+ * [Decomp] §5.1 (ring) and §5.4 (unroll-by-2, bidirectional); see
+ * coco_schedule. `order` is a host array of `nranks` int32 (caller-owned).
+ * nranks in 1..COCO_MAX_PTRS and 0 <= rank < nranks, else COCO_ERR_SHAPE;
+ * unknown kind or schedule: COCO_ERR_VALUE; NULL order: COCO_ERR_NULL.
+ * Host only; no CUDA call.
+ */
+coco_status coco_shard_order(int32_t kind, int32_t schedule, int32_t rank, int32_t nranks, int32_t* order);
+
+/*
+ * The cost model that enables the decomposition ([Decomp] §5.5, "cost model
+ * and enabling mechanism"): an AllGather-Einsum or Einsum-ReduceScatter is
+ * replaced by its Looped CollectiveEinsum only when it is expected to pay,
+ *     orig_comp + orig_comm >= max(orig_comp, ring_comm) + epilogue_cost,
+ * where orig_comp and orig_comm are the times of the original einsum and
+ * collective, ring_comm the time of the CollectivePermutes along the logical
+ * ring, and epilogue_cost the time of the prologue or epilogue the schedule
+ * adds (all in one unit). Writes 1 (decompose) or 0 (keep the original
+ * operations) to *profitable. Every time must be finite and >= 0, else
+ * COCO_ERR_VALUE (and *profitable is untouched); NULL: COCO_ERR_NULL. Host
+ * only; no CUDA call.
+ */
+coco_status coco_loop_profitable(double orig_comp, double orig_comm, double ring_comm, double epilogue_cost,
+                                 int32_t* profitable);
+
 /* ------------------------------------------------------------- utilities */
 
 /*

@@ -291,3 +291,76 @@ def test_noalloc_rejects_overflowing_extents_before_any_cuda_call(coco):
     o = mk(coco, F32, R, (0, 16), n, base=FAKE + (1 << 40))
     assert coco.raw_call("coco_allreduce_rs_ag_noalloc", ctypes.byref(t), ctypes.byref(o), None) == 0
     assert coco.raw_call("coco_allreduce_rs_ag_noalloc", None, ctypes.byref(o), None) == 1
+
+
+# ------------------------------------------- schedule query and cost model (host only)
+
+def _traced_orders(kind, sched, n):
+    """Per-rank orders read off the oracle's looped forms (shard IDs travel with the data there)."""
+    import numpy as np
+    import oracle
+    ones = [np.ones((n, n)) for _ in range(n)]
+    trace = []
+    if kind == 0:
+        if sched == 2:
+            oracle.looped_allgather_einsum_bidirectional("mk,kn->mn", "lhs", "m", [np.ones((1, n))] * n,
+                                                         [np.ones((n, n))] * n, trace)
+        else:
+            oracle.looped_allgather_einsum("mk,kn->mn", "lhs", "m", [np.ones((1, n))] * n, [np.ones((n, n))] * n,
+                                           trace)
+        return [[t[-1] for t in sorted(trace, key=lambda t: t[0]) if t[1] == r] for r in range(n)]
+    if sched == 0:
+        oracle.looped_einsum_reduce_scatter("mk,kn->mn", ones, ones, "m", trace)
+        return [[q for (i, q, sid) in sorted(trace) if sid == r] for r in range(n)]
+    if sched == 1:
+        oracle.looped_einsum_reduce_scatter_unrolled("mk,kn->mn", ones, ones, "m", trace)
+        return [[q for (i, q, c, sid) in sorted(trace) if sid == r and c == "A"] +
+                [q for (i, q, c, sid) in sorted(trace) if sid == r and c == "B"] for r in range(n)]
+    oracle.looped_einsum_reduce_scatter_bidirectional("mk,kn->mn", ones, ones, "m", trace)
+    return [[q for (i, q, d, sid) in sorted(trace) if sid == r and d == "left"] +
+            [q for (i, q, d, sid) in sorted(trace) if sid == r and d == "right"] + [r] for r in range(n)]
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8])
+def test_shard_order_matches_the_oracles_schedules(coco, n):
+    for kind in (0, 1):
+        for sched in (0, 1, 2):
+            want = _traced_orders(kind, sched, n)
+            for r in range(n):
+                got = coco.coco_shard_order(kind, sched, r, n)
+                assert got == want[r], (kind, sched, n, r)
+                assert sorted(got) == list(range(n))
+
+
+def test_shard_order_validation(coco):
+    NULL, SHAPE, VALUE = 1, 2, 10
+    arr = (ctypes.c_int32 * 8)()
+    assert coco.raw_call("coco_shard_order", 0, 0, 0, 8, None) == NULL
+    assert coco.raw_call("coco_shard_order", 0, 0, 8, 8, arr) == SHAPE
+    assert coco.raw_call("coco_shard_order", 0, 0, -1, 8, arr) == SHAPE
+    assert coco.raw_call("coco_shard_order", 0, 0, 0, 0, arr) == SHAPE
+    assert coco.raw_call("coco_shard_order", 0, 0, 0, 65, arr) == SHAPE
+    assert coco.raw_call("coco_shard_order", 2, 0, 0, 8, arr) == VALUE
+    assert coco.raw_call("coco_shard_order", 0, 3, 0, 8, arr) == VALUE
+
+
+def test_loop_profitable_matches_the_oracle(coco):
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(55)
+    vals = [0.0, 0.25, 1.0, 2.0, 3.0, 4.0]
+    cases = [(a, b, c, d) for a in vals for b in vals for c in vals for d in vals]
+    cases += [tuple(rng.uniform(0, 10, 4)) for _ in range(2000)]
+    for c in cases:
+        assert coco.coco_loop_profitable(*c) == oracle.loop_profitable(*c), c
+
+
+def test_loop_profitable_validation(coco):
+    NULL, VALUE = 1, 10
+    out = ctypes.c_int32(7)
+    for bad in [(-1.0, 0, 0, 0), (0, -1e-9, 0, 0), (0, 0, float("nan"), 0), (0, 0, 0, float("inf"))]:
+        assert coco.raw_call("coco_loop_profitable", *[ctypes.c_double(v) for v in bad],
+                             ctypes.byref(out)) == VALUE
+        assert out.value == 7  # untouched
+    assert coco.raw_call("coco_loop_profitable", *[ctypes.c_double(1.0)] * 4, None) == \
+        NULL
