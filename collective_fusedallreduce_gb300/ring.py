@@ -1,0 +1,395 @@
+"""The Looped CollectiveEinsum and the FusedAllReduce with one rank per device.
+
+In the rest of this package all N logical ranks live in one GPU's memory and a
+CollectivePermute is a read of the shard where it lives. Here every rank
+owns its buffers and the data really moves:
+
+* [Decomp] "Overlap Communication with Dependent Computation via
+  Decomposition in Large Deep Learning Models", §4 (Figs. 4 and 5) and §5.1
+  (Alg. 1): N iterations, each starting an asynchronous CollectivePermute
+  along the pairs {j -> j-1} into a local receive buffer (the double buffer
+  of §5.4.1), computing the partial einsum of the shard in hand while the
+  transfer runs, then waiting for it (CollectivePermuteDone). AllGather-
+  Einsum: cases 1, 2 and 3 of §5.1; Einsum-ReduceScatter: the accumulator
+  travels and each rank adds its partial for the shard ID it receives.
+* [Decomp] §5.5: the loop replaces the original collective + einsum only when
+  the cost model says it pays (coco_loop_profitable); otherwise the original
+  AllGather followed by one einsum runs.
+* [CoCoNet] "Breaking the Computation and Communication Abstraction Barrier
+  in Distributed Machine Learning Workloads", AllReduce Split and AllReduce
+  Fuse (§5.2): the FusedAllReduce as a ReduceScatter (every rank receives
+  slice r of every partial), the bias / dropout / residual on that slice
+  only, and an AllGather of the finished slices.
+
+The shard schedule is the library's (coco_shard_order), the one its
+single-GPU kernels follow, and the arithmetic of every step runs in the
+library's kernels through ``CocoCompute``; the transport only moves bytes.
+
+Transports:
+* ``DistTransport``: one rank per process over ``torch.distributed`` (NCCL
+  between GPUs, gloo between CPU processes). Point-to-point sends and
+  receives, all-to-all and all-gather; no multicast or NVLS.
+* ``LoopbackTransport``: all ranks in one process (their buffers in one
+  device's memory); a permute is a device copy. It runs the same loops as the
+  distributed form, so their schedule and arithmetic can be checked on one
+  GPU.
+
+Readings taken where the pages leave a step open:
+* The ReduceScatter's first iteration sends a zero accumulator; it carries no
+  data, so here iteration 0 writes its partial straight into the accumulator
+  and the first transfer happens at iteration 1 (same shard IDs, same sums).
+* The distributed Einsum-ReduceScatter accumulates in fp32 (the Addition of
+  §5.1 in the accumulator's type) and supports outputs partitioned on the
+  rows of the LHS; the FusedAllReduce sums the N slices in rank order 0..N-1
+  in fp32, exactly as coco_fused_allreduce does, so the two are bit for bit
+  equal.
+"""
+
+import torch
+
+from . import coco
+
+AG, RS = coco.AG_ORDER, coco.RS_ORDER
+
+
+# ------------------------------------------------------------------ transports
+
+
+class _Done:
+    """A started transfer; wait() is the CollectivePermuteDone."""
+
+    def __init__(self, works=()):
+        self._works = list(works)
+
+    def wait(self):
+        for w in self._works:
+            w.wait()
+        self._works = []
+
+
+class DistTransport:
+    """One rank per process over torch.distributed (the default process group or ``group``)."""
+
+    def __init__(self, group=None):
+        import torch.distributed as dist
+        self._dist = dist
+        self.group = group
+        self.nranks = dist.get_world_size(group)
+        self.rank = dist.get_rank(group)
+        self.local_ranks = [self.rank]
+
+    def _global(self, r):
+        return r if self.group is None else self._dist.get_global_rank(self.group, r)
+
+    def permute(self, send, recv, shift=1):
+        """Start a CollectivePermute: rank j's ``send`` lands in rank j-shift's ``recv``
+        ({j -> j-1} for shift 1). Returns a handle whose wait() completes it."""
+        if self.nranks == 1:
+            recv[0].copy_(send[0])
+            return _Done()
+        d = self._dist
+        ops = [d.P2POp(d.isend, send[0], self._global((self.rank - shift) % self.nranks), self.group),
+               d.P2POp(d.irecv, recv[0], self._global((self.rank + shift) % self.nranks), self.group)]
+        return _Done(d.batch_isend_irecv(ops))
+
+    def all_to_all(self, send, recv):
+        """Chunk s of recv[0] = chunk r of rank s's send[0] (r = this rank): both are flat tensors of N
+        equal chunks."""
+        if self.nranks == 1:
+            recv[0].copy_(send[0])
+            return
+        self._dist.all_to_all_single(recv[0], send[0], group=self.group)
+
+    def all_gather(self, src, dst):
+        """dst[0][s] = rank s's src."""
+        if self.nranks == 1:
+            dst[0][0].copy_(src[0])
+            return
+        self._dist.all_gather(list(dst[0]), src[0], group=self.group)
+
+
+class LoopbackTransport:
+    """All ranks in this process: the per-rank lists hold every rank's tensor."""
+
+    def __init__(self, nranks):
+        self.nranks = int(nranks)
+        self.rank = None
+        self.local_ranks = list(range(self.nranks))
+
+    def permute(self, send, recv, shift=1):
+        n = self.nranks
+        for j in range(n):
+            recv[(j - shift) % n].copy_(send[j])
+        return _Done()
+
+    def all_to_all(self, send, recv):
+        n = self.nranks
+        c = send[0].numel() // n
+        for r in range(n):
+            for s in range(n):
+                recv[r].narrow(0, s * c, c).copy_(send[s].narrow(0, r * c, c))
+
+    def all_gather(self, src, dst):
+        for r in range(self.nranks):
+            for s in range(self.nranks):
+                dst[r][s].copy_(src[s])
+
+
+# ----------------------------------------------------------------- compute
+
+
+class CocoCompute:
+    """The steps' arithmetic through the library's kernels (CUDA tensors only)."""
+
+    def __init__(self, stream=None):
+        self.stream = stream
+
+    @staticmethod
+    def _cuda(ts):
+        for t in ts:
+            if not t.is_cuda:
+                raise RuntimeError("CocoCompute runs the library's CUDA kernels: tensors must be on a GPU")
+
+    def einsum(self, spec, lhs, rhs, out):
+        """out[l] = lhs[l] @ rhs[l] for every local rank l (one launch)."""
+        self._cuda(lhs + rhs + out)
+        coco.coco_einsum(spec, coco.local(lhs), coco.local(rhs), coco.local(out), self.stream)
+
+    def accumulate(self, acc, part):
+        """acc[l] = acc[l] + part[l] in the accumulator's type (one launch: a two-rank sum per local rank)."""
+        self._cuda(acc + part)
+        n = len(acc)
+        ins = [t for pair in zip(acc, part) for t in pair]
+        outs = [t for a in acc for t in (a, a)]
+        coco.coco_allreduce(coco.local(ins, ngroups=n), coco.replicated(outs, ngroups=n), self.stream)
+
+    def assemble(self, chunks, dim, full):
+        """full = the chunks concatenated along ``dim`` in partition order (the AllGather's placement)."""
+        self._cuda(list(chunks) + [full])
+        n = len(chunks)
+        coco.coco_allgather(coco.sliced(list(chunks), dim), coco.replicated([full] * n), self.stream)
+
+    def fused_slice(self, slices, bias, residual, p, seed, index_base, out):
+        """out = dropout(sum over s of slices[s] + bias) + residual on one slice of the flattened tensor,
+        whose first element has whole-tensor index ``index_base``."""
+        self._cuda(list(slices) + [out] + ([residual] if residual is not None else []))
+        n = len(slices)
+        coco.coco_fused_allreduce_at(coco.local(list(slices)), bias,
+                                     None if residual is None else coco.replicated([residual] * n),
+                                     p, seed, index_base, coco.replicated([out] * n), self.stream)
+
+
+# ---------------------------------------------------------- the cost model
+
+
+def ring_times(flops, shard_bytes, nranks, tensor_tflops, ring_gbs, collective_gbs, epilogue_s=0.0):
+    """The four times of [Decomp] §5.5 from a plain bandwidth model: the einsum at the tensor rate, the
+    original collective moving (N-1) shards at ``collective_gbs`` (all links of the mesh), the ring moving
+    the same (N-1) shards over one link at ``ring_gbs``, and the prologue / epilogue cost given."""
+    comp = flops / (tensor_tflops * 1e12)
+    moved = (nranks - 1) * shard_bytes
+    return comp, moved / (collective_gbs * 1e9), moved / (ring_gbs * 1e9), epilogue_s
+
+
+def decompose(times):
+    """[Decomp] §5.5: decompose only if orig_comp + orig_comm >= max(orig_comp, ring_comm) + epilogue."""
+    return coco.coco_loop_profitable(*times)
+
+
+# ------------------------------------------------- Looped AllGather-Einsum
+
+
+def _dim(spec, operand, label):
+    lhs, rhs = spec.replace(" ", "").split("->")[0].split(",")
+    labels = lhs if operand == "lhs" else rhs
+    return labels.index(label)
+
+
+def looped_allgather_einsum(spec, looped, slice_label, shard, other, out, transport, compute, trace=None,
+                            gate=None):
+    """Rank r's out = einsum of the gathered looped operand with its own ``other`` operand, computed
+    as the Looped AllGather-Einsum ([Decomp] §5.1).
+
+    Per local rank l: ``shard[l]`` is its shard of the looped operand (``looped`` = "lhs" or "rhs",
+    sliced along ``slice_label``), ``other[l]`` its local operand, ``out[l]`` its output. Case 1
+    (non-contracting m / n): DynamicUpdateSlice of the shard's rows / columns of out; case 2
+    (contracting k): Addition into out (fp32); case 3 (batch b): DynamicUpdateSlice of its batches.
+    ``trace`` (a list) makes every transfer carry its shard ID beside the data and receives
+    (iteration, rank, shard_id) for each partial einsum. ``gate``: the four §5.5 times; when they say
+    the loop does not pay, the original AllGather and one einsum run instead.
+    """
+    if looped not in ("lhs", "rhs") or slice_label not in "bmnk" or len(slice_label) != 1:
+        raise ValueError("looped must be 'lhs' or 'rhs' and slice_label one of b, m, n, k")
+    if slice_label == "n" and looped == "lhs" or slice_label == "m" and looped == "rhs":
+        raise ValueError(f"{slice_label!r} is not a dimension of the {looped} operand")
+    n = transport.nranks
+    L = transport.local_ranks
+    sd = _dim(spec, looped, slice_label)
+    ext = shard[0].shape[sd]
+    if gate is not None and not decompose(gate):
+        return _allgather_then_einsum(spec, looped, sd, shard, other, out, transport, compute)
+
+    # receive buffers: two of our own, so the caller's shard is only ever read
+    spare = [[torch.empty_like(s) for s in shard] for _ in range(2 if n > 2 else 1)]
+    cur, nxt = list(shard), spare[0]
+    ids = nid = None
+    if trace is not None:
+        ids = [torch.full((1,), r, dtype=torch.int64, device=shard[0].device) for r in L]
+        nid = [torch.empty_like(t) for t in ids]
+    orders = [coco.coco_shard_order(AG, coco.SCHED_RING, r, n) for r in L]
+    acc_part = None
+    for i in range(n):
+        sids = [o[i] for o in orders]
+        h = hid = None
+        if i < n - 1:  # CollectivePermuteStart: the shard in hand goes to r-1, r+1's arrives
+            h = transport.permute(cur, nxt)
+            if ids is not None:
+                hid = transport.permute(ids, nid)
+        if ids is not None:
+            got = [int(t.item()) for t in ids]
+            if got != sids:
+                raise AssertionError(f"iteration {i}: shards {got} in hand, schedule says {sids}")
+            trace.extend((i, r, s) for r, s in zip(L, sids))
+        # the partial einsum of this iteration, on the shard in hand
+        if slice_label == "k":  # case 2: DynamicSlice of the other operand along k, Addition
+            od = _dim(spec, "rhs" if looped == "lhs" else "lhs", "k")
+            oth = [o.narrow(od, s * ext, ext) for o, s in zip(other, sids)]
+            if any(not t.is_contiguous() for t in oth):
+                raise ValueError("case 2 needs the other operand's k slices contiguous (k its leading dimension)")
+            lhs, rhs = (cur, oth) if looped == "lhs" else (oth, cur)
+            if i == 0:
+                compute.einsum(spec, lhs, rhs, out)
+            else:
+                if acc_part is None:
+                    acc_part = [torch.empty_like(o) for o in out]
+                compute.einsum(spec, lhs, rhs, acc_part)
+                compute.accumulate(out, acc_part)
+        else:
+            od = spec.replace(" ", "").split("->")[1].index(slice_label)
+            dst = [o.narrow(od, s * ext, ext) for o, s in zip(out, sids)]
+            if slice_label == "b":  # case 3: DynamicSlice of the other operand along b
+                ob = _dim(spec, "rhs" if looped == "lhs" else "lhs", "b")
+                oth = [o.narrow(ob, s * ext, ext) for o, s in zip(other, sids)]
+            else:
+                oth = list(other)
+            if any(not t.is_contiguous() for t in dst):
+                raise ValueError("the DynamicUpdateSlice target must be contiguous (slice on a leading dimension)")
+            lhs, rhs = (cur, oth) if looped == "lhs" else (oth, cur)
+            compute.einsum(spec, lhs, rhs, dst)
+        if h is not None:  # CollectivePermuteDone
+            h.wait()
+            cur, nxt = nxt, (spare[(i + 1) % 2] if len(spare) == 2 else cur)
+            if hid is not None:
+                hid.wait()
+                ids, nid = nid, ids
+    return out
+
+
+def _allgather_then_einsum(spec, looped, sd, shard, other, out, transport, compute):
+    """The original operations: AllGather of the looped operand, then one einsum."""
+    n = transport.nranks
+    full_shape = list(shard[0].shape)
+    full_shape[sd] *= n
+    full = [torch.empty(full_shape, dtype=shard[0].dtype, device=shard[0].device) for _ in shard]
+    chunks = [[torch.empty_like(shard[0]) for _ in range(n)] for _ in shard]
+    transport.all_gather(list(shard), chunks)
+    for c, f in zip(chunks, full):  # placed in partition order by the library's AllGather kernel
+        compute.assemble(c, sd, f)
+    lhs, rhs = (full, list(other)) if looped == "lhs" else (list(other), full)
+    compute.einsum(spec, lhs, rhs, out)
+    return out
+
+
+# ------------------------------------------------ Looped Einsum-ReduceScatter
+
+
+def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=None):
+    """Rank r's out = shard r (rows of the LHS) of the sum over ranks q of lhs_q @ rhs_q, computed as
+    the Looped Einsum-ReduceScatter ([Decomp] §5.1): the fp32 accumulator travels {j -> j-1}; at
+    iteration i rank q computes its partial for shard (q+i+1) mod N (a DynamicSlice of its LHS rows)
+    while the accumulator of that shard is on its way, then adds it. Output shard r collects the
+    ranks r-1, r-2, ..., r in that order. ``out[l]``: fp32 [M/N, ...] per local rank. ``trace``: as in
+    looped_allgather_einsum.
+    """
+    n = transport.nranks
+    L = transport.local_ranks
+    if out[0].dtype != torch.float32:
+        raise ValueError("the accumulator (and so the output) of the distributed ReduceScatter is fp32")
+    md = _dim(spec, "lhs", "m")
+    m = lhs[0].shape[md]
+    if m % n:
+        raise ValueError("the LHS rows do not split into equal shards")
+    ms = m // n
+    # the accumulator changes buffers at every iteration after the first: start it in the buffer
+    # that makes it end in ``out``
+    other_buf = [torch.empty_like(o) for o in out]
+    acc, inc = (list(out), other_buf) if n % 2 == 1 else (other_buf, list(out))
+    part = [torch.empty_like(o) for o in out]
+    ids = nid = None
+    if trace is not None:
+        ids = [torch.zeros((1,), dtype=torch.int64, device=out[0].device) for _ in L]
+        nid = [torch.empty_like(t) for t in ids]
+    for i in range(n):
+        sids = [(q + i + 1) % n for q in L]
+        h = hid = None
+        if i > 0:  # CollectivePermuteStart of the accumulators
+            h = transport.permute(acc, inc)
+            if ids is not None:
+                hid = transport.permute(ids, nid)
+        sl = [x.narrow(md, s * ms, ms) for x, s in zip(lhs, sids)]
+        compute.einsum(spec, sl, list(rhs), acc if i == 0 else part)
+        if i == 0:
+            if ids is not None:
+                for t, s in zip(ids, sids):
+                    t.fill_(s)
+        else:
+            h.wait()  # CollectivePermuteDone
+            if hid is not None:
+                hid.wait()
+                ids, nid = nid, ids
+            compute.accumulate(inc, part)
+            acc, inc = inc, acc
+        if ids is not None:
+            got = [int(t.item()) for t in ids]
+            if got != sids:
+                raise AssertionError(f"iteration {i}: accumulators {got} in hand, schedule says {sids}")
+            trace.extend((i, q, s) for q, s in zip(L, sids))
+    for a, o in zip(acc, out):  # after N iterations each rank holds its own shard
+        if a.data_ptr() != o.data_ptr():
+            o.copy_(a)
+    return out
+
+
+# ------------------------------------------------------ FusedAllReduce (split)
+
+
+def fused_allreduce(partial, bias, residual, p, seed, out, transport, compute):
+    """out = dropout(sum over ranks of partial + bias) + residual on every rank, as [CoCoNet]'s
+    AllReduce Split + Fuse: each rank receives slice r (of N equal slices of the flattened tensor) of
+    every rank's partial, sums them in rank order with the bias, dropout and residual of those elements
+    only (whole-tensor element indices, so the mask is the one-device mask), and the finished slices
+    are all-gathered. ``partial[l]``, ``residual[l]`` (or None), ``out[l]``: per local rank, one shape."""
+    n = transport.nranks
+    L = transport.local_ranks
+    numel = partial[0].numel()
+    vec = 16 // partial[0].element_size()
+    if numel % (n * vec):
+        raise ValueError(f"{numel} elements do not split into {n} slices of whole 16-byte vectors")
+    S = numel // n
+    H = partial[0].shape[-1]
+    if bias is not None and S % H:
+        raise ValueError("with a bias, every slice must hold whole rows of the last dimension")
+    shape = (S // H, H) if S % H == 0 else (S,)  # the bias runs along the last dimension
+    send = [x.reshape(-1) for x in partial]
+    recv = [torch.empty(numel, dtype=partial[0].dtype, device=partial[0].device) for _ in L]
+    transport.all_to_all(send, recv)  # ReduceScatter's data movement: slice r of every rank's partial
+    mine = []
+    for l, r in enumerate(L):
+        o = torch.empty(S, dtype=out[0].dtype, device=out[0].device)
+        res = None if residual is None else residual[l].reshape(-1).narrow(0, r * S, S).view(shape)
+        got = [recv[l].narrow(0, s * S, S).view(shape) for s in range(n)]
+        compute.fused_slice(got, bias, res, p, seed, r * S, o.view(shape))
+        mine.append(o)
+    dst = [[o.reshape(-1).narrow(0, s * S, S) for s in range(n)] for o in out]
+    transport.all_gather(mine, dst)  # AllGather of the finished slices
+    return out
