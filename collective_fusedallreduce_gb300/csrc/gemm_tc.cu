@@ -37,6 +37,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -803,9 +804,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
           }
         }
         // the strip about to be overwritten was handed to a bulk store two chunks ago (FusedAllReduce:
-        // its one output strip, to the stores of the previous chunk)
+        // its one output strip, to the stores of the previous chunk). Chunks stored with plain stores
+        // commit no bulk group, so after a bulk-stored tile the group count no longer tells which
+        // strip is free: such chunks wait for every earlier bulk store to have read its strip.
         if (lane == 0) {
-          if constexpr (MODE == EPI_FUSED_ALLREDUCE) bulk_wait_read_all();
+          if (MODE == EPI_FUSED_ALLREDUCE || !bulk) bulk_wait_read_all();
           else bulk_wait_read_le1();
         }
         __syncwarp();
@@ -867,6 +870,354 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
     __syncwarp();
     tc_fence_after();
     tmem_dealloc<TWO_SM>(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------ B-stationary short-K kernel
+//
+// Jobs that contract over at most BS_KB k-blocks (K <= 128, such as the
+// batched einsum of [Decomp] §5.1 case 3) are bound by their output stream: a
+// 128 x 256 tile's MMAs take about a quarter of the time its bf16 results
+// take to reach HBM. In k_gemm_tc each such tile also loads a 32 KB A tile
+// and a 64 KB B tile through the SM's TMA unit, which the stores share. Here
+// a CTA keeps one B tile [K x 256] in shared memory for a unit of up to
+// BS_MTILES vertically adjacent m-tiles and streams only their A tiles:
+// 48 KB of operand loads per output tile instead of 96 KB.
+//
+// One CTA per SM, no cluster. Warp 0 (one lane) loads B once per unit (two B
+// buffers, so the next unit's B arrives while this unit's MMAs run) and A
+// once per tile, warp 1 issues one M=128, N=256 MMA per K=16 step from an
+// elected lane into one of two TMEM accumulators, warps 2..5 store as in
+// k_gemm_tc (a ring of BS_STRIPS strips per warp). Units are numbered with
+// the n-tile innermost, so CTAs running side by side read the same A tiles,
+// and the two m-halves of a B tile are BS_MTILES units apart.
+constexpr int BS_KB = 2;
+constexpr int BS_MTILES = 4;
+constexpr int BS_B_BUFS = 2;
+constexpr int BS_A_STAGES = 2;
+constexpr int BS_STRIPS = 2;
+constexpr int BS_EPI_WARPS = 4;  // one per TMEM lane quarter (8, two per quarter, measured 6 % slower)
+constexpr int BS_B_TILE = BS_KB * B_BYTES;  // 64 KB
+constexpr int BS_A_TILE = BS_KB * A_BYTES;  // 32 KB
+struct BsCfg {
+  static constexpr int EPI_WARPS = BS_EPI_WARPS;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int A_OFF = BS_B_BUFS * BS_B_TILE;
+  static constexpr int EPI_OFF = A_OFF + BS_A_STAGES * BS_A_TILE;
+  static constexpr int BAR_OFF = EPI_OFF + EPI_WARPS * BS_STRIPS * EPI_STRIP;
+  // B full x bufs, B empty x bufs, A full x stages, A empty x stages, TMEM full x2, TMEM empty x2, drain
+  static constexpr int NUM_BARS = 2 * BS_B_BUFS + 2 * BS_A_STAGES + 5;
+  static constexpr int SMEM_BYTES = BAR_OFF + 8 * NUM_BARS + 16 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory over the per-CTA limit");
+};
+
+// At most N committed bulk groups may still be reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_le() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+struct BsUnit {
+  int job, bb, mt0, ntm, nt;
+};
+
+// Unit u of a B-stationary launch: (job, batch, m-chunk, n-tile), n-tile innermost.
+__device__ __forceinline__ BsUnit bs_decode(const TcParams& P, int u) {
+  int lo = 0, hi = P.njobs - 1;
+  while (lo < hi) {  // last job with unit_start <= u
+    const int mid = (lo + hi + 1) >> 1;
+    if (P.unit_start[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  const int mtiles = (P.jobs[lo].m + BM - 1) / BM, ntiles = (P.jobs[lo].n + BN - 1) / BN;
+  const int mch = (mtiles + BS_MTILES - 1) / BS_MTILES;
+  const int local = u - P.unit_start[lo];
+  const int per_b = mch * ntiles;
+  BsUnit U;
+  U.job = lo;
+  U.bb = local / per_b;
+  const int r = local - U.bb * per_b;
+  const int mc = r / ntiles;
+  U.nt = r - mc * ntiles;
+  U.mt0 = mc * BS_MTILES;
+  U.ntm = min(BS_MTILES, mtiles - U.mt0);
+  return U;
+}
+
+__global__ void __launch_bounds__(BsCfg::THREADS, 1) k_gemm_tc_bs(const __grid_constant__ TcParams P) {
+  constexpr int A_OFF = BsCfg::A_OFF, EPI_OFF = BsCfg::EPI_OFF, BAR_OFF = BsCfg::BAR_OFF;
+  constexpr int NUM_BARS = BsCfg::NUM_BARS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + BAR_OFF;
+  constexpr uint32_t ABAR = 16u * BS_B_BUFS;  // offset of the A barriers
+  auto bfull = [&](int b) { return bar0 + 8u * b; };
+  auto bempty = [&](int b) { return bar0 + 8u * (BS_B_BUFS + b); };
+  auto afull = [&](int s) { return bar0 + ABAR + 8u * s; };
+  auto aempty = [&](int s) { return bar0 + ABAR + 8u * (BS_A_STAGES + s); };
+  auto tfull = [&](int a) { return bar0 + ABAR + 8u * (2 * BS_A_STAGES + a); };
+  auto tempty = [&](int a) { return bar0 + ABAR + 8u * (2 * BS_A_STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + ABAR + 8u * (2 * BS_A_STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 8 * NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 8 * NUM_BARS + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < BS_B_BUFS; ++b) {
+      mbar_init(bfull(b), 1);
+      mbar_init(bempty(b), 1);
+    }
+    for (int s = 0; s < BS_A_STAGES; ++s) {
+      mbar_init(afull(s), 1);
+      mbar_init(aempty(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), BsCfg::EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) tmem_alloc<false>(smem_u32(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicCAS(P.err, 0u, static_cast<unsigned int>(COCO_ERR_TIMEOUT));
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------- TMA producer (lane 0)
+    if (lane == 0) {
+      int bb_ = 0;  // B buffer of the next unit
+      uint32_t bphase = 0;
+      uint32_t b_issued = 0, b_parity = 0;  // per B buffer: a copy was issued, and the phase it completes
+      int st = 0;
+      uint32_t aph = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per A stage: a copy was issued, and the phase it completes
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+        const BsUnit U = bs_decode(P, u);
+        const Job J = P.jobs[U.job];
+        // the unit's B tile: every k-block of every segment, in segment order
+        if (!mbar_wait(bempty(bb_), bphase ^ 1u, abort_flag)) {
+          fail();
+          ok = false;
+          break;
+        }
+        mbar_expect_tx(bfull(bb_), static_cast<uint32_t>(J.kblocks * B_BYTES));
+        {
+          const uint32_t sbt = sbase + bb_ * BS_B_TILE;
+          int kb = 0;
+          for (int si = 0; si < J.nseg; ++si) {
+            const Seg S = P.segs[J.seg0 + si];
+            const int kbs = (S.klen + BK - 1) / BK;
+            for (int k = 0; k < kbs; ++k, ++kb)
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_3d(sbt + kb * B_BYTES + j * B_BOX_BYTES, &P.maps[S.b], bfull(bb_),
+                            S.b_c0 + U.nt * BN + 64 * j, S.b_k0 + k * BK, S.b_b0 + U.bb);
+          }
+        }
+        b_issued |= 1u << bb_;
+        b_parity = (b_parity & ~(1u << bb_)) | (bphase << bb_);
+        if (++bb_ == BS_B_BUFS) { bb_ = 0; bphase ^= 1u; }
+        // its m-tiles' A tiles
+        for (int t = 0; t < U.ntm; ++t) {
+          if (!mbar_wait(aempty(st), aph ^ 1u, abort_flag)) {
+            fail();
+            ok = false;
+            break;
+          }
+          const uint32_t sa = sbase + A_OFF + st * BS_A_TILE;
+          mbar_expect_tx(afull(st), static_cast<uint32_t>(J.kblocks * A_BYTES));
+          int kb = 0;
+          for (int si = 0; si < J.nseg; ++si) {
+            const Seg S = P.segs[J.seg0 + si];
+            const int kbs = (S.klen + BK - 1) / BK;
+            for (int k = 0; k < kbs; ++k, ++kb)
+              tma_load_3d(sa + kb * A_BYTES, &P.maps[S.a], afull(st), S.a_k0 + k * BK,
+                          S.a_r0 + (U.mt0 + t) * BM, S.a_b0 + U.bb);
+          }
+          issued |= 1u << st;
+          issued_parity = (issued_parity & ~(1u << st)) | (aph << st);
+          if (++st == BS_A_STAGES) { st = 0; aph ^= 1u; }
+        }
+      }
+      if (!ok) {  // let copies in flight land before the CTA's shared memory goes away
+        int dummy = 0;
+        volatile int* never = &dummy;
+        for (int b = 0; b < BS_B_BUFS; ++b)
+          if ((b_issued >> b) & 1u) mbar_wait(bfull(b), (b_parity >> b) & 1u, never);
+        for (int s = 0; s < BS_A_STAGES; ++s)
+          if ((issued >> s) & 1u) mbar_wait(afull(s), (issued_parity >> s) & 1u, never);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = elect_one();
+    const uint32_t idesc = P.idesc;
+    int bb_ = 0;
+    uint32_t bphase = 0;
+    int st = 0;
+    uint32_t aph = 0;
+    int lt = 0;  // tiles of this CTA so far
+    bool ok = true, any_mma = false;
+    for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+      const BsUnit U = bs_decode(P, u);
+      const int kblocks = P.jobs[U.job].kblocks;
+      if (!mbar_wait_warp(bfull(bb_), bphase, abort_flag)) {
+        if (leader) fail();
+        ok = false;
+        break;
+      }
+      const uint32_t sbt = sbase + bb_ * BS_B_TILE;
+      tc_fence_after();
+      for (int t = 0; t < U.ntm; ++t, ++lt) {
+        const int acc = lt & 1;
+        const uint32_t tph = (lt >> 1) & 1;
+        if (!mbar_wait_warp(tempty(acc), tph ^ 1u, abort_flag) || !mbar_wait_warp(afull(st), aph, abort_flag)) {
+          if (leader) fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        if (leader) {
+          for (int kb = 0; kb < kblocks; ++kb) {
+            const uint64_t ad = desc_a(sbase + A_OFF + st * BS_A_TILE + kb * A_BYTES);
+            const uint64_t bd = desc_b(sbt + kb * B_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) umma(d, ad + 2 * k, bd + 128 * k, idesc, (kb | k) != 0);
+          }
+          umma_commit(aempty(st));  // the A stage may be refilled
+          umma_commit(tfull(acc));  // the epilogue may read the accumulator
+        }
+        __syncwarp();
+        any_mma = true;
+        if (++st == BS_A_STAGES) { st = 0; aph ^= 1u; }
+      }
+      if (ok && leader) umma_commit(bempty(bb_));  // the unit's B buffer may be refilled
+      __syncwarp();
+      if (++bb_ == BS_B_BUFS) { bb_ = 0; bphase ^= 1u; }
+    }
+    if (!ok && any_mma) {  // wait for the MMAs already issued before TMEM is freed
+      if (leader) umma_commit(drain_bar);
+      __syncwarp();
+      int dummy = 0;
+      volatile int* never = &dummy;
+      mbar_wait_warp(drain_bar, 0, never);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    const uint32_t strips = sbase + EPI_OFF + (warp - 2) * BS_STRIPS * EPI_STRIP;
+    constexpr int COLS = BN / (BsCfg::EPI_WARPS / 4);  // columns of a tile this warp stores
+    const int col_begin = ((warp - 2) >> 2) * COLS;
+    uint64_t evict_first = 0;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(evict_first));
+    const int out_dt = P.out_dtype;
+    const int esize = out_dt == COCO_F32 ? 4 : 2;
+    const int cols_per_chunk = 128 / esize;
+    const int vec_elems = 16 / esize;
+    int lt = 0, buf = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < P.total_units; u += gridDim.x) {
+      const BsUnit U = bs_decode(P, u);
+      const Job J = P.jobs[U.job];
+      const OutView O = P.outs[J.out];
+      const int64_t obatch = static_cast<int64_t>(J.o_b0 + U.bb) * O.bstride;
+      for (int t = 0; t < U.ntm; ++t, ++lt) {
+        const int mt = U.mt0 + t;
+        const int acc = lt & 1;
+        const uint32_t tph = (lt >> 1) & 1;
+        const int row0 = mt * BM + quarter * 32;  // job-relative row of this warp's lane 0
+        const bool ready = __all_sync(0xffffffffu, mbar_wait(tfull(acc), tph, abort_flag));
+        if (!ready) {
+          if (lane == 0) fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+        const bool bulk = (mt * BM + BM <= J.m || J.o_r0 + J.m == O.rows) &&
+                          (U.nt * BN + BN <= J.n || J.o_c0 + J.n == O.cols);
+        for (int c0 = col_begin; c0 < col_begin + COLS; c0 += cols_per_chunk) {
+          const bool last = c0 + cols_per_chunk >= col_begin + COLS;
+          uint32_t p[32];
+          if (out_dt == COCO_F32) {
+            tmem_ld32(tbase + c0, p);
+            tmem_ld_wait();
+          } else {
+            uint32_t r[32], r2[32];
+            tmem_ld32(tbase + c0, r);
+            tmem_ld32(tbase + c0 + 32, r2);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              p[i] = cvt_pair(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]), out_dt);
+              p[16 + i] = cvt_pair(__uint_as_float(r2[2 * i]), __uint_as_float(r2[2 * i + 1]), out_dt);
+            }
+          }
+          if (last) {  // this warp's part of the accumulator is in registers: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed(tempty(acc));
+          }
+          // the strip about to be overwritten was handed to a bulk store BS_STRIPS chunks ago; chunks
+          // stored with plain stores commit no group, so they wait for every earlier bulk store
+          if (lane == 0) {
+            if (bulk) bulk_wait_read_le<BS_STRIPS - 1>();
+            else bulk_wait_read_all();
+          }
+          __syncwarp();
+          const uint32_t strip = strips + buf * EPI_STRIP;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)  // row = lane, 16-byte chunk c at its 128-byte-swizzle slot
+            st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2],
+                         p[4 * c + 3]);
+          if (bulk) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&P.omaps[J.out], strip, J.o_c0 + U.nt * BN + c0, J.o_r0 + row0, J.o_b0 + U.bb,
+                           evict_first);
+              bulk_commit();
+            }
+          } else {
+            __syncwarp();
+            // strip -> global: 8 lanes per 128-byte row segment, 4 rows per pass, bounded by the job
+            const int ch = lane & 7;
+            const int col = U.nt * BN + c0 + ch * vec_elems;  // job-relative column
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int rr = it * 4 + (lane >> 3);
+              const int row = row0 + rr;
+              const uint4 v = ld_shared_v4(strip + rr * 128 + ((ch ^ (rr & 7)) << 4));
+              if (row < J.m && col < J.n) {
+                const int64_t off = obatch + static_cast<int64_t>(J.o_r0 + row) * O.ld + (J.o_c0 + col);
+                *reinterpret_cast<uint4*>(static_cast<char*>(O.ptr) + off * esize) = v;
+              }
+            }
+            __syncwarp();
+          }
+          if (++buf == BS_STRIPS) buf = 0;
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();  // bulk stores finish before the CTA's shared memory goes away
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<false>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -963,7 +1314,7 @@ bool encode_out(CUtensorMap* map, const OutView& o, int dtype) {
 
 // per kernel variant and device: the dynamic shared-memory limit was raised (static storage: starts false;
 // atomic because calls may come from several host threads, which at worst both set the attribute)
-std::atomic<bool> smem_configured[4][64];
+std::atomic<bool> smem_configured[5][64];
 
 }  // namespace
 
@@ -982,7 +1333,22 @@ unsigned int* gemm_error_word() {
 
 // Splits the plan into launches that fit the parameter block, remapping view,
 // segment and output indices, then launches each.
-cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* err_word) {
+// Plans are turned into launches in two steps: tc_prepare encodes every
+// tensor map and fills the parameter blocks (host work only, no stream
+// operation), tc_launch enqueues them. A prepared plan may be launched any
+// number of times; only the error word and the arrival counter of a
+// cooperative launch are set per launch.
+struct TcPrepared {
+  void (*kernel)(TcParams) = nullptr;
+  int smem = 0, threads = 0;
+  std::vector<std::unique_ptr<TcParams>> params;  // one per launch (wave_sync: the launch wants it)
+  std::vector<int> grids;
+};
+
+void tc_free(TcPrepared* p) { delete p; }
+
+cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out) {
+  *out = nullptr;
   if (!encode_fn()) return cudaErrorNotSupported;
   const bool far = plan.mode == EPI_FUSED_ALLREDUCE;
   if (far && plan.out_dtype == COCO_F32) return cudaErrorNotSupported;
@@ -1004,10 +1370,18 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
   for (const Job& J : plan.jobs)
     for (int k = 0; k < J.nseg; ++k) kb_sum += (plan.segs[J.seg0 + k].klen + BK - 1) / BK;
   const bool two_sm = plan.jobs.empty() ? true : kb_sum >= static_cast<int64_t>(kTwoSmMinKBlocks) * plan.jobs.size();
-  const int variant = (far ? 2 : 0) + (two_sm ? 1 : 0);
+  // jobs of at most BS_KB k-blocks are store-bound: the B-stationary kernel halves their operand loads
+  bool bs = !far && !plan.jobs.empty();
+  for (const Job& J : plan.jobs) {
+    int kb = 0;
+    for (int k = 0; k < J.nseg; ++k) kb += (plan.segs[J.seg0 + k].klen + BK - 1) / BK;
+    bs = bs && kb <= BS_KB;
+  }
+  const int variant = bs ? 4 : (far ? 2 : 0) + (two_sm ? 1 : 0);
   void (*kernel)(TcParams) = nullptr;
   int smem = 0, threads = 0;
   switch (variant) {
+    case 4: kernel = k_gemm_tc_bs; smem = BsCfg::SMEM_BYTES; threads = BsCfg::THREADS; break;
     case 0: kernel = k_gemm_tc<EPI_STORE, false>; smem = Cfg<EPI_STORE, false>::SMEM_BYTES;
             threads = Cfg<EPI_STORE, false>::THREADS; break;
     case 1: kernel = k_gemm_tc<EPI_STORE, true>; smem = Cfg<EPI_STORE, true>::SMEM_BYTES;
@@ -1026,16 +1400,21 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
   }
   // A-views are used with the A box and B-views with the B box; a view used
   // on both sides gets two maps.
-  TcParams* P = new TcParams;
+  std::unique_ptr<TcPrepared> prep(new TcPrepared);
+  prep->kernel = kernel;
+  prep->smem = smem;
+  prep->threads = threads;
   cudaError_t status = cudaSuccess;
   size_t j = 0;
   const int fmt = plan.in_dtype == COCO_BF16 ? 1 : 0;
   // instruction descriptor: f32 accumulator, A and B of the input type, A K-major, B N-major,
   // N = 256, M = 128 per CTA (256 for the pair MMA)
-  const uint32_t mma_m = two_sm ? 2 * BM : BM;
+  const uint32_t mma_m = two_sm && !bs ? 2 * BM : BM;
   const uint32_t idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (0u << 15) | (1u << 16) |
                          (static_cast<uint32_t>(BN >> 3) << 17) | ((mma_m >> 4) << 24);
   while (j < plan.jobs.size() && status == cudaSuccess) {
+    std::unique_ptr<TcParams> Pown(new TcParams);
+    TcParams* P = Pown.get();
     memset(P, 0, sizeof(TcParams));
     std::vector<int> amap(plan.views.size(), -1), bmap(plan.views.size(), -1);
     std::vector<std::pair<int, int>> orange;  // (first output, count) ranges already in this launch
@@ -1096,7 +1475,10 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
       if (nj.kblocks <= 0) { status = cudaErrorInvalidValue; break; }  // an empty contraction is zero-filled, not run
       P->jobs[njobs] = nj;
       P->unit_start[njobs] = tiles;
-      tiles += J.nb * ((J.m + 2 * BM - 1) / (2 * BM)) * ((J.n + BN - 1) / BN);
+      if (bs)  // units of up to BS_MTILES m-tiles sharing one B tile
+        tiles += J.nb * ((J.m + BS_MTILES * BM - 1) / (BS_MTILES * BM)) * ((J.n + BN - 1) / BN);
+      else  // units of two vertically adjacent tiles, one per CTA of the pair
+        tiles += J.nb * ((J.m + 2 * BM - 1) / (2 * BM)) * ((J.n + BN - 1) / BN);
       ++njobs;
       ++j;
     }
@@ -1122,28 +1504,42 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
       P->group_pairs = (bmax <= (int64_t(64) << 20) && kbmin >= 64) ? 1 : GROUP_M / 2;
       // the grouped raster on long k-loops re-reads operands from DRAM when the pairs of a wave drift
       // apart; the pair-MMA launch then keeps its producers in step (a cooperative launch)
-      P->wave_sync = (two_sm && P->group_pairs != 1 && kbmin >= 64) ? 1 : 0;
+      P->wave_sync = (two_sm && !bs && P->group_pairs != 1 && kbmin >= 64) ? 1 : 0;
     }
     P->total_units = tiles;
     P->idesc = idesc;
     P->out_dtype = plan.out_dtype;
-    P->err = err_word;
+    P->err = nullptr;  // set per launch
     P->bias = plan.far.bias;
     P->seed = plan.far.seed;
     P->keep_threshold = plan.far.keep_threshold;
     P->scale = plan.far.scale;
     P->dropout = plan.far.dropout ? 1 : 0;
-    const int pairs = sm_count() / 2;  // persistent: one CTA pair per two SMs
-    const int grid = 2 * (tiles < pairs ? tiles : pairs);
+    const int pairs = sm_count() / 2;  // persistent: one CTA pair per two SMs (B-stationary: one CTA per SM)
+    prep->grids.push_back(bs ? (tiles < sm_count() ? tiles : sm_count()) : 2 * (tiles < pairs ? tiles : pairs));
+    prep->params.push_back(std::move(Pown));
+  }
+  if (status != cudaSuccess) return status;
+  *out = prep.release();
+  return cudaSuccess;
+}
+
+cudaError_t tc_launch(TcPrepared* prep, cudaStream_t s, unsigned int* err_word) {
+  cudaError_t status = cudaSuccess;
+  for (size_t i = 0; i < prep->params.size() && status == cudaSuccess; ++i) {
+    TcParams* P = prep->params[i].get();
+    const int grid = prep->grids[i];
+    P->err = err_word;
+    const int32_t want_sync = P->wave_sync;
     bool launched = false;
-    if (P->wave_sync) {
+    if (want_sync) {
       void* base = nullptr;
       if (cudaGetSymbolAddress(&base, g_wave_counters) == cudaSuccess) {
         P->wave_counter = static_cast<unsigned int*>(base) + (g_wave_slot.fetch_add(1) % kWaveSlots);
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(threads);
-        cfg.dynamicSmemBytes = smem;
+        cfg.blockDim = dim3(prep->threads);
+        cfg.dynamicSmemBytes = prep->smem;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident at once: they wait on each other
@@ -1151,20 +1547,29 @@ cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* e
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaMemsetAsync(P->wave_counter, 0, sizeof(unsigned int), s) == cudaSuccess &&
-            cudaLaunchKernelEx(&cfg, kernel, *P) == cudaSuccess)
+            cudaLaunchKernelEx(&cfg, prep->kernel, *P) == cudaSuccess)
           launched = true;
       }
       (void)cudaGetLastError();  // a refused cooperative launch falls back to the plain one below
     }
     if (!launched) {
-      P->wave_sync = 0;
-      kernel<<<grid, threads, smem, s>>>(*P);
+      P->wave_sync = 0;  // the block is copied at launch: the prepared request is restored below
+      prep->kernel<<<grid, prep->threads, prep->smem, s>>>(*P);
+      P->wave_sync = want_sync;
     }
     count_launch();
     status = cudaGetLastError();
   }
-  delete P;
   return status;
+}
+
+cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* err_word) {
+  TcPrepared* prep = nullptr;
+  cudaError_t e = tc_prepare(plan, &prep);
+  if (e != cudaSuccess) return e;
+  e = tc_launch(prep, s, err_word);
+  tc_free(prep);
+  return e;
 }
 
 cudaError_t launch_wait_selftest(uint64_t timeout_ns, cudaStream_t s, unsigned int* err_word) {

@@ -133,6 +133,14 @@ struct GemmPlan {
 // Tensor-core path (bf16 / f16 inputs, tcgen05 + TMA). Returns
 // cudaErrorNotSupported if the plan violates a TMA rule the host checks.
 cudaError_t launch_gemm_tc(const GemmPlan& plan, cudaStream_t s, unsigned int* err_word);
+// The same in two steps: tc_prepare encodes the tensor maps and fills the
+// parameter blocks (host only; *out is freed with tc_free), tc_launch
+// enqueues them on `s` (any number of times; calls on one prepared plan must
+// not run concurrently, as each sets the per-launch fields of its blocks).
+struct TcPrepared;
+cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out);
+cudaError_t tc_launch(TcPrepared* prep, cudaStream_t s, unsigned int* err_word);
+void tc_free(TcPrepared* prep);
 // fp32 path (FMA units).
 cudaError_t launch_gemm_simt(const GemmPlan& plan, cudaStream_t s);
 
