@@ -111,6 +111,10 @@ _lib.coco_shard_order.restype = ctypes.c_int
 _lib.coco_loop_profitable.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                       ctypes.POINTER(ctypes.c_int32)]
 _lib.coco_loop_profitable.restype = ctypes.c_int
+_lib.coco_plan_cache_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64)] * 3
+_lib.coco_plan_cache_stats.restype = None
+_lib.coco_plan_cache_clear.argtypes = []
+_lib.coco_plan_cache_clear.restype = None
 
 EXPORTED = [
     "coco_fused_allreduce", "coco_fused_allreduce_at", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
@@ -119,7 +123,7 @@ EXPORTED = [
     "coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched", "coco_dropout_keep_mask",
     "coco_scattered_table_bytes", "coco_scattered_table_build", "coco_scattered_allreduce",
     "coco_device_status", "coco_wait_selftest", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
-    "coco_shard_order", "coco_loop_profitable",
+    "coco_shard_order", "coco_loop_profitable", "coco_plan_cache_stats", "coco_plan_cache_clear",
 ]
 
 
@@ -333,3 +337,14 @@ def coco_loop_profitable(orig_comp, orig_comm, ring_comm, epilogue_cost):
     _check(_lib.coco_loop_profitable(float(orig_comp), float(orig_comm), float(ring_comm), float(epilogue_cost),
                                      ctypes.byref(out)), "coco_loop_profitable")
     return bool(out.value)
+
+
+def coco_plan_cache_stats():
+    """(hits, misses, entries) of the library's plan cache."""
+    h, m, e = ctypes.c_uint64(), ctypes.c_uint64(), ctypes.c_uint64()
+    _lib.coco_plan_cache_stats(ctypes.byref(h), ctypes.byref(m), ctypes.byref(e))
+    return int(h.value), int(m.value), int(e.value)
+
+
+def coco_plan_cache_clear():
+    _lib.coco_plan_cache_clear()

@@ -10,6 +10,9 @@
 
 #include <atomic>
 #include <algorithm>
+#include <list>
+#include <memory>
+#include <mutex>
 #include <set>
 #include <cmath>
 #include <cstring>
@@ -267,6 +270,155 @@ coco_status run_plan(const GemmPlan& P, cudaStream_t s) {
   cudaError_t e = launch_gemm_tc(P, s, err);
   if (e == cudaErrorNotSupported) return COCO_ERR_UNSUPPORTED;
   return cuda_status(e);
+}
+
+// ------------------------------------------------------------ plan cache
+//
+// A call's plan (validated, with its tensor maps encoded) depends only on its
+// arguments: the entry point, the spec and schedule, the fields of every
+// coco_tensor argument that are in use (dtype, layout, shape, slice dim, rank
+// and group counts, pointers), the fused epilogue's scalars and the current
+// device. The cache keys each plan on exactly those, so a call that repeats
+// them (a training loop calling the same shapes every step) skips
+// validation, planning and tensor-map encoding. Only calls that passed
+// validation are entered, and the device is read (a CUDA call) only for
+// arguments that match an entry or have just passed validation, so invalid
+// arguments are still refused before any CUDA call. The stream is not part
+// of a plan. Least recently used entries beyond kPlanCacheSize are dropped.
+constexpr size_t kPlanCacheSize = 64;
+
+struct PlanKey {
+  std::vector<uint64_t> w;
+  bool ok = true;  // false: the arguments cannot be keyed (left to validation)
+  explicit PlanKey(uint64_t entry) {
+    w.reserve(256);
+    w.push_back(entry);
+  }
+  void add(uint64_t v) { w.push_back(v); }
+  void f32(float v) {
+    uint32_t b;
+    std::memcpy(&b, &v, 4);
+    w.push_back(b);
+  }
+  void str(const char* s) {
+    if (!s) { ok = false; return; }
+    uint64_t word = 0;
+    int i = 0;
+    for (; s[i] && i < 64; ++i) {
+      word = (word << 8) | static_cast<uint8_t>(s[i]);
+      if ((i & 7) == 7) { w.push_back(word); word = 0; }
+    }
+    if (s[i]) { ok = false; return; }  // longer than any spec the library takes
+    w.push_back(word);
+    w.push_back(static_cast<uint64_t>(i));
+  }
+  void tensor(const coco_tensor* t) {
+    if (!t) { w.push_back(~0ull); return; }
+    if (t->ndim < 1 || t->ndim > COCO_MAX_DIMS || t->nranks < 1 || t->ngroups < 1 ||
+        static_cast<int64_t>(t->nranks) * t->ngroups > COCO_MAX_PTRS) {
+      ok = false;
+      return;
+    }
+    w.push_back((static_cast<uint64_t>(static_cast<uint32_t>(t->dtype)) << 32) | static_cast<uint32_t>(t->layout));
+    w.push_back((static_cast<uint64_t>(static_cast<uint32_t>(t->ndim)) << 32) | static_cast<uint32_t>(t->slice_dim));
+    w.push_back((static_cast<uint64_t>(static_cast<uint32_t>(t->nranks)) << 32) | static_cast<uint32_t>(t->ngroups));
+    for (int d = 0; d < t->ndim; ++d) w.push_back(static_cast<uint64_t>(t->shape[d]));
+    for (int i = 0; i < t->nranks * t->ngroups; ++i) w.push_back(reinterpret_cast<uintptr_t>(t->ptr[i]));
+  }
+};
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return dev;
+}
+
+struct PlanEntry {
+  std::vector<uint64_t> key;
+  int device = -1;
+  GemmPlan plan;
+  bool tma_ok = false;
+  std::mutex m;  // launches of one entry set the per-launch fields of its parameter blocks
+  TcPrepared* tc = nullptr;
+  ~PlanEntry() {
+    if (tc) tc_free(tc);
+  }
+};
+
+class PlanCache {
+ public:
+  std::shared_ptr<PlanEntry> find(const std::vector<uint64_t>& key) {
+    std::lock_guard<std::mutex> g(m_);
+    int dev = -2;  // read once, and only when the arguments match an entry
+    for (auto it = lru_.begin(); it != lru_.end(); ++it)
+      if ((*it)->key == key && (*it)->device == (dev == -2 ? (dev = current_device()) : dev)) {
+        if (it != lru_.begin()) lru_.splice(lru_.begin(), lru_, it);
+        hits_.fetch_add(1, std::memory_order_relaxed);
+        return lru_.front();
+      }
+    misses_.fetch_add(1, std::memory_order_relaxed);
+    return nullptr;
+  }
+  std::shared_ptr<PlanEntry> insert(std::vector<uint64_t> key, GemmPlan&& plan, bool tma) {
+    auto e = std::make_shared<PlanEntry>();
+    e->key = std::move(key);
+    e->device = current_device();
+    e->plan = std::move(plan);
+    e->tma_ok = tma;
+    std::lock_guard<std::mutex> g(m_);
+    lru_.push_front(e);
+    while (lru_.size() > kPlanCacheSize) lru_.pop_back();  // in-use entries live on in their callers
+    return e;
+  }
+  void clear() {
+    std::lock_guard<std::mutex> g(m_);
+    lru_.clear();
+  }
+  void stats(uint64_t* hits, uint64_t* misses, uint64_t* entries) {
+    std::lock_guard<std::mutex> g(m_);
+    if (hits) *hits = hits_.load();
+    if (misses) *misses = misses_.load();
+    if (entries) *entries = lru_.size();
+  }
+
+ private:
+  std::mutex m_;
+  std::list<std::shared_ptr<PlanEntry>> lru_;  // most recently used first
+  std::atomic<uint64_t> hits_{0}, misses_{0};
+};
+
+PlanCache& plan_cache() {
+  static PlanCache* c = new PlanCache;  // never destroyed: calls may come during process exit
+  return *c;
+}
+
+// Runs a cached plan: the fp32 path launches from the plan; the tensor-core path encodes its maps
+// once (the first run of the entry) and relaunches the prepared parameter blocks after that.
+coco_status run_entry(PlanEntry& e, cudaStream_t s) {
+  const GemmPlan& P = e.plan;
+  if (P.jobs.empty()) return COCO_OK;
+  if (P.in_dtype == COCO_F32) return cuda_status(launch_gemm_simt(P, s));
+  if (!e.tma_ok) return COCO_ERR_ALIGN;
+  unsigned int* err = gemm_error_word();
+  if (!err) return cuda_status(cudaErrorSymbolNotFound);
+  std::lock_guard<std::mutex> g(e.m);
+  if (!e.tc) {
+    cudaError_t x = tc_prepare(P, &e.tc);
+    if (x == cudaErrorNotSupported) return COCO_ERR_UNSUPPORTED;
+    if (x != cudaSuccess) return cuda_status(x);
+  }
+  return cuda_status(tc_launch(e.tc, s, err));
+}
+
+// Enters a validated plan under `key` (when the call could be keyed) and runs it.
+coco_status run_keyed(GemmPlan&& P, const PlanKey& key, cudaStream_t s) {
+  if (!key.ok) return run_plan(P, s);
+  const bool tma = P.in_dtype == COCO_F32 || tma_ok(P);
+  std::shared_ptr<PlanEntry> e = plan_cache().insert(key.w, std::move(P), tma);
+  return run_entry(*e, s);
 }
 
 // Output pointers of a group that need computing: every rank for LOCAL, the
@@ -646,7 +798,7 @@ const void* operand_ptr(const TInfo& t, int g, int r) {
   return t.layout == COCO_REPLICATED ? t.ptr(g, 0) : t.ptr(g, r);
 }
 
-coco_status finish(GemmPlan& P, const EinsumArgs& E, int64_t k_total, void* stream) {
+coco_status finish(GemmPlan& P, const EinsumArgs& E, int64_t k_total, const PlanKey& key, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (E.out.numel == 0) return COCO_OK;
   coco_status st;
@@ -654,13 +806,29 @@ coco_status finish(GemmPlan& P, const EinsumArgs& E, int64_t k_total, void* stre
   if (k_total == 0) return zero_outputs(E.out, s);
   P.in_dtype = E.lhs.dtype;
   P.out_dtype = E.out.dtype;
-  return run_plan(P, s);
+  return run_keyed(std::move(P), key, s);
+}
+
+// The cached plan of a call with these arguments, run; false if there is none.
+bool run_cached(const PlanKey& key, void* stream, coco_status* st) {
+  if (!key.ok) return false;
+  std::shared_ptr<PlanEntry> e = plan_cache().find(key.w);
+  if (!e) return false;
+  *st = run_entry(*e, static_cast<cudaStream_t>(stream));
+  return true;
 }
 
 }  // namespace
 
 COCO_EXPORT coco_status coco_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
                                     const coco_tensor* out, void* stream) {
+  PlanKey key(1);
+  key.str(spec);
+  key.tensor(lhs);
+  key.tensor(rhs);
+  key.tensor(out);
+  coco_status cst;
+  if (run_cached(key, stream, &cst)) return cst;
   EinsumArgs E;
   coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
   if (st != COCO_OK) return st;
@@ -682,12 +850,23 @@ COCO_EXPORT coco_status coco_einsum(const char* spec, const coco_tensor* lhs, co
                                 add_view(&P, make_view(operand_ptr(E.rhs, g, r), b)), a.c));
       P.jobs.push_back(J);
     }
-  return finish(P, E, a.c, stream);
+  return finish(P, E, a.c, key, stream);
 }
 
 COCO_EXPORT coco_status coco_matmul_fused_allreduce(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
                                                     const void* bias, const coco_tensor* residual, float dropout_p,
                                                     uint64_t seed, const coco_tensor* out, void* stream) {
+  PlanKey key(2);
+  key.str(spec);
+  key.tensor(lhs);
+  key.tensor(rhs);
+  key.add(reinterpret_cast<uintptr_t>(bias));
+  key.tensor(residual);
+  key.f32(dropout_p);
+  key.add(seed);
+  key.tensor(out);
+  coco_status cst;
+  if (run_cached(key, stream, &cst)) return cst;
   EinsumArgs E;
   coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
   if (st != COCO_OK) return st;
@@ -759,7 +938,7 @@ COCO_EXPORT coco_status coco_matmul_fused_allreduce(const char* spec, const coco
                                 add_view(&P, make_view(E.rhs.ptr(g, r), b)), a.c));
     P.jobs.push_back(J);
   }
-  return run_plan(P, static_cast<cudaStream_t>(stream));
+  return run_keyed(std::move(P), key, static_cast<cudaStream_t>(stream));
 }
 
 namespace {
@@ -808,6 +987,14 @@ bool valid_schedule(int sched) { return sched >= COCO_SCHED_RING && sched <= COC
 coco_status looped_ag_einsum(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs, const coco_tensor* out,
                              int sched, void* stream) {
   if (!valid_schedule(sched)) return COCO_ERR_VALUE;
+  PlanKey key(3);
+  key.add(static_cast<uint64_t>(sched));
+  key.str(spec);
+  key.tensor(lhs);
+  key.tensor(rhs);
+  key.tensor(out);
+  coco_status cst;
+  if (run_cached(key, stream, &cst)) return cst;
   EinsumArgs E;
   coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
   if (st != COCO_OK) return st;
@@ -899,12 +1086,20 @@ coco_status looped_ag_einsum(const char* spec, const coco_tensor* lhs, const coc
       }
     }
   }
-  return finish(P, E, A.c, stream);
+  return finish(P, E, A.c, key, stream);
 }
 
 coco_status looped_einsum_rs(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs, const coco_tensor* out,
                              int sched, void* stream) {
   if (!valid_schedule(sched)) return COCO_ERR_VALUE;
+  PlanKey key(4);
+  key.add(static_cast<uint64_t>(sched));
+  key.str(spec);
+  key.tensor(lhs);
+  key.tensor(rhs);
+  key.tensor(out);
+  coco_status cst;
+  if (run_cached(key, stream, &cst)) return cst;
   EinsumArgs E;
   coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
   if (st != COCO_OK) return st;
@@ -939,7 +1134,7 @@ coco_status looped_einsum_rs(const char* spec, const coco_tensor* lhs, const coc
       P.jobs.push_back(J);
     }
   }
-  return finish(P, E, a.c, stream);
+  return finish(P, E, a.c, key, stream);
 }
 
 }  // namespace
@@ -984,3 +1179,9 @@ COCO_EXPORT coco_status coco_loop_profitable(double orig_comp, double orig_comm,
   *profitable = orig_comp + orig_comm >= std::max(orig_comp, ring_comm) + epilogue_cost ? 1 : 0;
   return COCO_OK;
 }
+
+COCO_EXPORT void coco_plan_cache_stats(uint64_t* hits, uint64_t* misses, uint64_t* entries) {
+  plan_cache().stats(hits, misses, entries);
+}
+
+COCO_EXPORT void coco_plan_cache_clear(void) { plan_cache().clear(); }

@@ -439,6 +439,22 @@ coco_status coco_wait_selftest(uint64_t timeout_ns, void* stream);
  */
 uint64_t coco_kernel_launches(void);
 
+/*
+ * Plan cache of the einsum entry points (coco_einsum, coco_matmul_fused_allreduce,
+ * coco_looped_ag_einsum[_sched], coco_looped_einsum_rs[_sched]). A call whose
+ * arguments repeat an earlier valid call's exactly (entry point, spec,
+ * schedule, every in-use field of every coco_tensor including its pointers,
+ * bias pointer, dropout_p, seed, and the current device) reuses that call's
+ * plan and encoded tensor maps, skipping host validation and planning; the
+ * stream may differ. Up to 64 plans are kept (least recently used dropped),
+ * in host memory only. Freeing a buffer and passing a new one at the same
+ * address with the same shape is safe: a plan depends only on the keyed
+ * values. Counters are cumulative for the process; clear() drops every plan
+ * (not the counters). Both are thread-safe; NULL arguments are skipped.
+ */
+void coco_plan_cache_stats(uint64_t* hits, uint64_t* misses, uint64_t* entries);
+void coco_plan_cache_clear(void);
+
 /* The cudaError_t (as int) of the most recent COCO_ERR_CUDA on this thread. */
 int coco_last_cuda_error(void);
 

@@ -364,3 +364,56 @@ def test_loop_profitable_validation(coco):
         assert out.value == 7  # untouched
     assert coco.raw_call("coco_loop_profitable", *[ctypes.c_double(1.0)] * 4, None) == \
         NULL
+
+
+def test_plan_cache_keys_on_every_argument(coco):
+    """A repeated call finds its plan; any changed pointer, shape, dtype, spec or schedule misses. Runs
+    without a GPU: the keyed plans are entered after validation, and the status of a call that hits is
+    the status of the call that made the plan (here the missing device's error, the same both times)."""
+    B16, L, S = coco.BF16, coco.LOCAL, coco.SLICED
+    coco.coco_plan_cache_clear()
+    lhs = mk(coco, B16, S, (64, 32), 4, slice_dim=0)
+    rhs = mk(coco, B16, L, (32, 16), 4, base=FAKE + (1 << 40))
+    out = mk(coco, B16, L, (64, 16), 4, base=FAKE + (1 << 41))
+    A = "coco_looped_ag_einsum"
+
+    def delta(fn):
+        h0, m0, _ = coco.coco_plan_cache_stats()
+        st = fn()
+        h1, m1, e1 = coco.coco_plan_cache_stats()
+        return st, h1 - h0, m1 - m0, e1
+
+    first, h, m, e = delta(lambda: ein(coco, A, b"mk,kn->mn", lhs, rhs, out))
+    assert (h, m, e) == (0, 1, 1)
+    again, h, m, e = delta(lambda: ein(coco, A, b"mk,kn->mn", lhs, rhs, out))
+    assert (again, h, m, e) == (first, 1, 0, 1)
+    # a changed pointer of one rank, a changed shape, another spec spelling, a schedule, an entry point
+    moved = mk(coco, B16, L, (32, 16), 4, base=FAKE + (1 << 40))
+    moved.ptr[3] = FAKE + (1 << 40) + 3 * (1 << 32) + 4096
+    _, h, m, _ = delta(lambda: ein(coco, A, b"mk,kn->mn", lhs, moved, out))
+    assert (h, m) == (0, 1)
+    lhs2 = mk(coco, B16, S, (128, 32), 4, slice_dim=0)
+    out2 = mk(coco, B16, L, (128, 16), 4, base=FAKE + (1 << 41))
+    _, h, m, _ = delta(lambda: ein(coco, A, b"mk,kn->mn", lhs2, rhs, out2))
+    assert (h, m) == (0, 1)
+    _, h, m, _ = delta(lambda: ein(coco, A, b"mk, kn->mn", lhs, rhs, out))
+    assert (h, m) == (0, 1)
+    _, h, m, _ = delta(lambda: coco.raw_call("coco_looped_ag_einsum_sched", b"mk,kn->mn", ctypes.byref(lhs),
+                                             ctypes.byref(rhs), ctypes.byref(out), 2, None))
+    assert (h, m) == (0, 1)
+    f16 = mk(coco, coco.F16, S, (64, 32), 4, slice_dim=0)
+    _, h, m, _ = delta(lambda: ein(coco, A, b"mk,kn->mn", f16, mk(coco, coco.F16, L, (32, 16), 4,
+                                                                  base=FAKE + (1 << 40)),
+                                   mk(coco, coco.F16, L, (64, 16), 4, base=FAKE + (1 << 41))))
+    assert (h, m) == (0, 1)
+    # the original arguments still hit; a stream is not part of a plan
+    _, h, m, _ = delta(lambda: coco.raw_call(A, b"mk,kn->mn", ctypes.byref(lhs), ctypes.byref(rhs),
+                                             ctypes.byref(out), ctypes.c_void_p(0x1234)))
+    assert (h, m) == (1, 0)
+    # invalid calls are never entered
+    _, _, _, e0 = delta(lambda: None)
+    bad, h, m, e = delta(lambda: ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, B16, L, (16, 16), 4,
+                                                                          base=FAKE + (1 << 41))))
+    assert bad == 2 and e == e0
+    coco.coco_plan_cache_clear()
+    assert coco.coco_plan_cache_stats()[2] == 0
