@@ -14,7 +14,8 @@ owns its buffers and the data really moves:
   travels and each rank adds its partial for the shard ID it receives.
 * [Decomp] §5.5: the loop replaces the original collective + einsum only when
   the cost model says it pays (coco_loop_profitable); otherwise the original
-  AllGather followed by one einsum runs.
+  operations run (AllGather then one einsum, or the einsum then a
+  ReduceScatter).
 * [CoCoNet] "Breaking the Computation and Communication Abstraction Barrier
   in Distributed Machine Learning Workloads", AllReduce Split and AllReduce
   Fuse (§5.2): the FusedAllReduce as a ReduceScatter (every rank receives
@@ -303,13 +304,14 @@ def _allgather_then_einsum(spec, looped, sd, shard, other, out, transport, compu
 # ------------------------------------------------ Looped Einsum-ReduceScatter
 
 
-def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=None):
+def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=None, gate=None):
     """Rank r's out = shard r (rows of the LHS) of the sum over ranks q of lhs_q @ rhs_q, computed as
     the Looped Einsum-ReduceScatter ([Decomp] §5.1): the fp32 accumulator travels {j -> j-1}; at
     iteration i rank q computes its partial for shard (q+i+1) mod N (a DynamicSlice of its LHS rows)
     while the accumulator of that shard is on its way, then adds it. Output shard r collects the
     ranks r-1, r-2, ..., r in that order. ``out[l]``: fp32 [M/N, ...] per local rank. ``trace``: as in
-    looped_allgather_einsum.
+    looped_allgather_einsum. ``gate``: the four §5.5 times; when they say the loop does not pay, the
+    original operations run: each rank's whole einsum, then a ReduceScatter of the results.
     """
     n = transport.nranks
     L = transport.local_ranks
@@ -320,6 +322,8 @@ def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=
     if m % n:
         raise ValueError("the LHS rows do not split into equal shards")
     ms = m // n
+    if gate is not None and not decompose(gate):
+        return _einsum_then_reduce_scatter(spec, lhs, rhs, out, transport, compute)
     # the accumulator changes buffers at every iteration after the first: start it in the buffer
     # that makes it end in ``out``
     other_buf = [torch.empty_like(o) for o in out]
@@ -357,6 +361,22 @@ def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=
     for a, o in zip(acc, out):  # after N iterations each rank holds its own shard
         if a.data_ptr() != o.data_ptr():
             o.copy_(a)
+    return out
+
+
+def _einsum_then_reduce_scatter(spec, lhs, rhs, out, transport, compute):
+    """The original operations: every rank's whole einsum (fp32), then a ReduceScatter onto the LHS rows
+    (an all-to-all of the row shards, summed in rank order by the library's reduction kernel)."""
+    n = transport.nranks
+    L = transport.local_ranks
+    shape = list(out[0].shape)
+    full = [torch.empty([shape[0] * n] + shape[1:], dtype=torch.float32, device=out[0].device) for _ in L]
+    compute.einsum(spec, list(lhs), list(rhs), full)
+    S = out[0].numel()
+    recv = [torch.empty(S * n, dtype=torch.float32, device=out[0].device) for _ in L]
+    transport.all_to_all([f.reshape(-1) for f in full], recv)  # shard r of every rank's result to rank r
+    for l, o in enumerate(out):
+        compute.fused_slice([recv[l].narrow(0, s * S, S).view(o.shape) for s in range(n)], None, None, 0.0, 0, 0, o)
     return out
 
 

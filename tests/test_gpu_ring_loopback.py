@@ -136,3 +136,33 @@ def test_split_fused_allreduce_is_bit_identical(dtype):
         assert torch.equal(a, b)
     want = oracle.fused_allreduce(_f64(parts), synth.as_f64(bias), synth.as_f64(res), 0.1, 99)
     assert_close(out[0], want, dtype, "split FusedAllReduce")
+
+
+def test_reduce_scatter_gate_keeps_the_original_einsum_then_reduce_scatter():
+    n, ms, k, nn = 4, 128, 192, 256
+    lhs = [t.to(DEV) for t in synth.per_rank(307, 0, n, (n * ms, k), torch.bfloat16, "smallint")]
+    rhs = [t.to(DEV) for t in synth.per_rank(307, 1, n, (k, nn), torch.bfloat16, "smallint")]
+    T, C = ring.LoopbackTransport(n), ring.CocoCompute()
+    looped = [torch.empty((ms, nn), dtype=torch.float32, device=DEV) for _ in range(n)]
+    kept = [torch.empty_like(o) for o in looped]
+    ring.looped_einsum_reduce_scatter("mk,kn->mn", lhs, rhs, looped, T, C, gate=(2.0, 1.0, 1.0, 0.0))
+    ring.looped_einsum_reduce_scatter("mk,kn->mn", lhs, rhs, kept, T, C, gate=(1.0, 1.0, 5.0, 0.0))
+    torch.cuda.synchronize()
+    for a, b in zip(looped, kept):
+        assert torch.equal(a, b)  # small integers: every sum exact in either order
+
+
+def test_case3_ring_with_the_looped_operand_on_the_right():
+    n, b, m, k, nn = 4, 2, 256, 128, 256
+    lhs = [t.to(DEV) for t in synth.per_rank(308, 0, n, (n * b, m, k), torch.bfloat16)]
+    shards = [t.to(DEV) for t in synth.per_rank(308, 1, n, (b, k, nn), torch.bfloat16)]
+    out = [torch.empty((n * b, m, nn), dtype=torch.bfloat16, device=DEV) for _ in range(n)]
+    ring.looped_allgather_einsum("bmk,bkn->bmn", "rhs", "b", shards, lhs, out, ring.LoopbackTransport(n),
+                                 ring.CocoCompute())
+    ref = [torch.empty_like(o) for o in out]
+    coco.coco_looped_ag_einsum("bmk,bkn->bmn", coco.local(lhs), coco.sliced(shards, 0), coco.local(ref))
+    coco.coco_device_status()
+    want = oracle.looped_allgather_einsum("bmk,bkn->bmn", "rhs", "b", _f64(shards), _f64(lhs))
+    for a, r, w in zip(out, ref, want):
+        assert torch.equal(a, r)
+        assert_close(a, w, torch.bfloat16, "ring case 3, looped RHS")

@@ -131,6 +131,9 @@ def _run(rank, world, port, q):
         want = oracle.looped_einsum_reduce_scatter("mk,kn->mn", [f64(a) for a in x["rs_lhs"]],
                                                    [f64(b) for b in x["rs_rhs"]], "m", otrace)[rank]
         res["rs"] = (bool(np.array_equal(f64(out[0]), want)), sorted(trace) == sorted(t for t in otrace if t[1] == rank))
+        kept = [torch.zeros((2, 4))]
+        ring.looped_einsum_reduce_scatter("mk,kn->mn", [x["rs_lhs"][rank]], [x["rs_rhs"][rank]], kept, T, C, gate=keep)
+        res["rs_gated"] = (bool(np.array_equal(f64(kept[0]), want)), True)
 
         out = [torch.empty((2 * world, 16))]
         ring.fused_allreduce([x["far_partials"][rank]], x["far_bias"], [x["far_res"]], 0.25, 1234, out, T, C)
