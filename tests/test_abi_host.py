@@ -417,3 +417,38 @@ def test_plan_cache_keys_on_every_argument(coco):
     assert bad == 2 and e == e0
     coco.coco_plan_cache_clear()
     assert coco.coco_plan_cache_stats()[2] == 0
+
+
+def test_plan_cache_under_concurrent_calls(coco):
+    """Several host threads calling with the same and with different arguments at once: every call gets
+    the status a single call gets, and the cache's counters account for every keyed call."""
+    import threading
+    B16, L, S = coco.BF16, coco.LOCAL, coco.SLICED
+    coco.coco_plan_cache_clear()
+    h0, m0, _ = coco.coco_plan_cache_stats()
+    rhs = mk(coco, B16, L, (32, 16), 4, base=FAKE + (1 << 40))
+    calls = []
+    for t in range(8):
+        lhs = mk(coco, B16, S, (64, 32), 4, slice_dim=0)
+        out = mk(coco, B16, L, (64, 16), 4, base=FAKE + (1 << 41) + (t % 3) * (1 << 36))  # three distinct keys
+        calls.append((lhs, out))
+    want = ein(coco, "coco_looped_ag_einsum", b"mk,kn->mn", calls[0][0], rhs, calls[0][1])
+    statuses, errors = [], []
+
+    def worker(lhs, out):
+        try:
+            for _ in range(50):
+                statuses.append(ein(coco, "coco_looped_ag_einsum", b"mk,kn->mn", lhs, rhs, out))
+        except Exception as e:  # pragma: no cover
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=c) for c in calls]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors
+    assert set(statuses) == {want} and len(statuses) == 400
+    h1, m1, e1 = coco.coco_plan_cache_stats()
+    assert (h1 - h0) + (m1 - m0) == 401 and e1 >= 3
+    coco.coco_plan_cache_clear()
