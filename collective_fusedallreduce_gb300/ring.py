@@ -206,8 +206,48 @@ def _dim(spec, operand, label):
     return labels.index(label)
 
 
+class _Chain:
+    """Data travelling around the ring in one direction: the tensors in hand on every local rank, the
+    buffers the next transfer lands in (two of the chain's own, so a caller's tensor is only read), and,
+    in trace mode, an ID carried beside the data. ``shift`` 1 moves data {j -> j-1}, -1 {j -> j+1},
+    2 two hops {j -> j-2}."""
+
+    def __init__(self, first, shift, transport, first_ids=None):
+        self.t = transport
+        self.shift = shift
+        self.cur = list(first)
+        self.spare = [[torch.empty_like(x) for x in first] for _ in range(2)]
+        self.nxt = self.spare[0]
+        self.k = 0
+        self.ids = None
+        if first_ids is not None:
+            dev = first[0].device
+            self.ids = [torch.full((1,), int(v), dtype=torch.int64, device=dev) for v in first_ids]
+            self.nid = [torch.empty_like(x) for x in self.ids]
+
+    def start(self):  # CollectivePermuteStart
+        h = self.t.permute(self.cur, self.nxt, self.shift)
+        hid = self.t.permute(self.ids, self.nid, self.shift) if self.ids is not None else None
+        return h, hid
+
+    def done(self, hs):  # CollectivePermuteDone: the received data is now in hand
+        h, hid = hs
+        h.wait()
+        self.k += 1
+        self.cur, self.nxt = self.nxt, self.spare[self.k % 2]
+        if hid is not None:
+            hid.wait()
+            self.ids, self.nid = self.nid, self.ids
+
+    def check(self, want, what):
+        if self.ids is not None:
+            got = [int(x.item()) for x in self.ids]
+            if got != list(want):
+                raise AssertionError(f"{what}: IDs {got} in hand, schedule says {list(want)}")
+
+
 def looped_allgather_einsum(spec, looped, slice_label, shard, other, out, transport, compute, trace=None,
-                            gate=None):
+                            gate=None, schedule=None):
     """Rank r's out = einsum of the gathered looped operand with its own ``other`` operand, computed
     as the Looped AllGather-Einsum ([Decomp] §5.1).
 
@@ -215,14 +255,21 @@ def looped_allgather_einsum(spec, looped, slice_label, shard, other, out, transp
     sliced along ``slice_label``), ``other[l]`` its local operand, ``out[l]`` its output. Case 1
     (non-contracting m / n): DynamicUpdateSlice of the shard's rows / columns of out; case 2
     (contracting k): Addition into out (fp32); case 3 (batch b): DynamicUpdateSlice of its batches.
+    ``schedule``: coco.SCHED_RING (default; unrolling by 2 is the same loop here, its double buffering
+    being the chain's two receive buffers, [Decomp] §5.4.1) or coco.SCHED_BIDIRECTIONAL ([Decomp]
+    §5.4.2: a prologue on the own shard, then each step receives shard r+k from one side and r-k from
+    the other and computes both).
     ``trace`` (a list) makes every transfer carry its shard ID beside the data and receives
-    (iteration, rank, shard_id) for each partial einsum. ``gate``: the four §5.5 times; when they say
+    (step, rank, shard_id) for each partial einsum. ``gate``: the four §5.5 times; when they say
     the loop does not pay, the original AllGather and one einsum run instead.
     """
     if looped not in ("lhs", "rhs") or slice_label not in "bmnk" or len(slice_label) != 1:
         raise ValueError("looped must be 'lhs' or 'rhs' and slice_label one of b, m, n, k")
     if slice_label == "n" and looped == "lhs" or slice_label == "m" and looped == "rhs":
         raise ValueError(f"{slice_label!r} is not a dimension of the {looped} operand")
+    sched = coco.SCHED_RING if schedule is None else int(schedule)
+    if sched not in (coco.SCHED_RING, coco.SCHED_UNROLL2, coco.SCHED_BIDIRECTIONAL):
+        raise ValueError(f"unknown schedule {schedule!r}")
     n = transport.nranks
     L = transport.local_ranks
     sd = _dim(spec, looped, slice_label)
@@ -230,59 +277,80 @@ def looped_allgather_einsum(spec, looped, slice_label, shard, other, out, transp
     if gate is not None and not decompose(gate):
         return _allgather_then_einsum(spec, looped, sd, shard, other, out, transport, compute)
 
-    # receive buffers: two of our own, so the caller's shard is only ever read
-    spare = [[torch.empty_like(s) for s in shard] for _ in range(2 if n > 2 else 1)]
-    cur, nxt = list(shard), spare[0]
-    ids = nid = None
-    if trace is not None:
-        ids = [torch.full((1,), r, dtype=torch.int64, device=shard[0].device) for r in L]
-        nid = [torch.empty_like(t) for t in ids]
-    orders = [coco.coco_shard_order(AG, coco.SCHED_RING, r, n) for r in L]
-    acc_part = None
-    for i in range(n):
-        sids = [o[i] for o in orders]
-        h = hid = None
-        if i < n - 1:  # CollectivePermuteStart: the shard in hand goes to r-1, r+1's arrives
-            h = transport.permute(cur, nxt)
-            if ids is not None:
-                hid = transport.permute(ids, nid)
-        if ids is not None:
-            got = [int(t.item()) for t in ids]
-            if got != sids:
-                raise AssertionError(f"iteration {i}: shards {got} in hand, schedule says {sids}")
-            trace.extend((i, r, s) for r, s in zip(L, sids))
-        # the partial einsum of this iteration, on the shard in hand
+    scratch = []
+    used = [0]  # partial einsums done (case 2: the first one writes out, the others add)
+
+    def partial(held, sids, step):
+        """The partial einsum of one shard per local rank: held[l] is shard sids[l] of the looped operand."""
+        if trace is not None:
+            trace.extend((step, r, sid) for r, sid in zip(L, sids))
         if slice_label == "k":  # case 2: DynamicSlice of the other operand along k, Addition
             od = _dim(spec, "rhs" if looped == "lhs" else "lhs", "k")
-            oth = [o.narrow(od, s * ext, ext) for o, s in zip(other, sids)]
+            oth = [o.narrow(od, sid * ext, ext) for o, sid in zip(other, sids)]
             if any(not t.is_contiguous() for t in oth):
                 raise ValueError("case 2 needs the other operand's k slices contiguous (k its leading dimension)")
-            lhs, rhs = (cur, oth) if looped == "lhs" else (oth, cur)
-            if i == 0:
+            lhs, rhs = (held, oth) if looped == "lhs" else (oth, held)
+            if used[0] == 0:
                 compute.einsum(spec, lhs, rhs, out)
             else:
-                if acc_part is None:
-                    acc_part = [torch.empty_like(o) for o in out]
-                compute.einsum(spec, lhs, rhs, acc_part)
-                compute.accumulate(out, acc_part)
+                if not scratch:
+                    scratch.extend(torch.empty_like(o) for o in out)
+                compute.einsum(spec, lhs, rhs, scratch)
+                compute.accumulate(out, scratch)
         else:
             od = spec.replace(" ", "").split("->")[1].index(slice_label)
-            dst = [o.narrow(od, s * ext, ext) for o, s in zip(out, sids)]
+            dst = [o.narrow(od, sid * ext, ext) for o, sid in zip(out, sids)]
             if slice_label == "b":  # case 3: DynamicSlice of the other operand along b
                 ob = _dim(spec, "rhs" if looped == "lhs" else "lhs", "b")
-                oth = [o.narrow(ob, s * ext, ext) for o, s in zip(other, sids)]
+                oth = [o.narrow(ob, sid * ext, ext) for o, sid in zip(other, sids)]
             else:
                 oth = list(other)
             if any(not t.is_contiguous() for t in dst):
                 raise ValueError("the DynamicUpdateSlice target must be contiguous (slice on a leading dimension)")
-            lhs, rhs = (cur, oth) if looped == "lhs" else (oth, cur)
+            lhs, rhs = (held, oth) if looped == "lhs" else (oth, held)
             compute.einsum(spec, lhs, rhs, dst)
-        if h is not None:  # CollectivePermuteDone
-            h.wait()
-            cur, nxt = nxt, (spare[(i + 1) % 2] if len(spare) == 2 else cur)
-            if hid is not None:
-                hid.wait()
-                ids, nid = nid, ids
+        used[0] += 1
+
+    orders = [coco.coco_shard_order(AG, sched if sched == coco.SCHED_BIDIRECTIONAL else coco.SCHED_RING, r, n)
+              for r in L]
+    own_ids = list(L) if trace is not None else None
+    if sched != coco.SCHED_BIDIRECTIONAL:
+        ch = _Chain(shard, 1, transport, own_ids)
+        for i in range(n):
+            sids = [o[i] for o in orders]
+            h = ch.start() if i < n - 1 else None  # the shard in hand goes to r-1, r+1's arrives
+            ch.check(sids, f"step {i}")
+            partial(ch.cur, sids, i)
+            if h is not None:
+                ch.done(h)
+        return out
+
+    # bidirectional: the own shard, then one shard from each side per step
+    left = _Chain(shard, 1, transport, own_ids)    # brings r+1, r+2, ...
+    right = _Chain(shard, -1, transport, own_ids)  # brings r-1, r-2, ...
+    pos = 0
+    step = 0
+    while pos < n:
+        take = 1 if pos == 0 else min(2, n - pos)  # shards computed in this step
+        after = pos + take
+        # the next step takes shard r+(step+1) from the left and, if two remain, r-(step+1) from the right
+        hl = left.start() if after < n else None
+        hr = right.start() if n - after >= 2 else None
+        if pos == 0:
+            left.check([o[0] for o in orders], "prologue")
+            partial(left.cur, [o[0] for o in orders], 0)
+        else:
+            left.check([o[pos] for o in orders], f"step {step} (left)")
+            partial(left.cur, [o[pos] for o in orders], step)
+            if take == 2:
+                right.check([o[pos + 1] for o in orders], f"step {step} (right)")
+                partial(right.cur, [o[pos + 1] for o in orders], step)
+        if hl is not None:
+            left.done(hl)
+        if hr is not None:
+            right.done(hr)
+        pos = after
+        step += 1
     return out
 
 
@@ -304,19 +372,74 @@ def _allgather_then_einsum(spec, looped, sd, shard, other, out, transport, compu
 # ------------------------------------------------ Looped Einsum-ReduceScatter
 
 
-def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=None, gate=None):
+class _Acc:
+    """An fp32 accumulator travelling around the ring (one chain of an Einsum-ReduceScatter): the tensor
+    in hand on every local rank (added to in place), the buffer the next transfer lands in, and, in trace
+    mode, the ID of the output shard it collects."""
+
+    def __init__(self, bufs, shift, transport, trace_mode):
+        self.acc, self.inc = bufs
+        self.shift = shift
+        self.t = transport
+        self.ids = self.nid = None
+        if trace_mode:
+            dev = self.acc[0].device
+            self.ids = [torch.zeros((1,), dtype=torch.int64, device=dev) for _ in self.acc]
+            self.nid = [torch.empty_like(x) for x in self.ids]
+
+    def start(self):  # CollectivePermuteStart
+        h = self.t.permute(self.acc, self.inc, self.shift)
+        hid = self.t.permute(self.ids, self.nid, self.shift) if self.ids is not None else None
+        return h, hid
+
+    def done(self, hs):  # CollectivePermuteDone
+        h, hid = hs
+        h.wait()
+        self.acc, self.inc = self.inc, self.acc
+        if hid is not None:
+            hid.wait()
+            self.ids, self.nid = self.nid, self.ids
+
+    def tag(self, sids):
+        if self.ids is not None:
+            for x, s_ in zip(self.ids, sids):
+                x.fill_(s_)
+
+    def check(self, sids, what):
+        if self.ids is not None:
+            got = [int(x.item()) for x in self.ids]
+            if got != list(sids):
+                raise AssertionError(f"{what}: accumulators {got} in hand, schedule says {list(sids)}")
+
+
+def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=None, gate=None, schedule=None):
     """Rank r's out = shard r (rows of the LHS) of the sum over ranks q of lhs_q @ rhs_q, computed as
-    the Looped Einsum-ReduceScatter ([Decomp] §5.1): the fp32 accumulator travels {j -> j-1}; at
-    iteration i rank q computes its partial for shard (q+i+1) mod N (a DynamicSlice of its LHS rows)
-    while the accumulator of that shard is on its way, then adds it. Output shard r collects the
-    ranks r-1, r-2, ..., r in that order. ``out[l]``: fp32 [M/N, ...] per local rank. ``trace``: as in
-    looped_allgather_einsum. ``gate``: the four §5.5 times; when they say the loop does not pay, the
-    original operations run: each rank's whole einsum, then a ReduceScatter of the results.
+    the Looped Einsum-ReduceScatter ([Decomp] §5.1): fp32 accumulators travel the ring; each rank
+    computes its partial for the shard ID of an accumulator while that accumulator is on its way, then
+    adds it. ``schedule``:
+
+    * coco.SCHED_RING (default): one accumulator {j -> j-1}; at iteration i rank q adds its partial for
+      shard (q+i+1) mod N; output shard r collects the ranks r-1, r-2, ..., r.
+    * coco.SCHED_UNROLL2 ([Decomp] §5.4.1): two interleaved chains travelling two hops per iteration,
+      chain A collecting ranks r-1, r-3, ... and chain B ranks r-2, r-4, ...; the chain that ends one
+      hop short takes one more hop and rank r adds the two.
+    * coco.SCHED_BIDIRECTIONAL ([Decomp] §5.4.2): a left-moving accumulator collects ranks r+a, ..., r+1
+      and a right-moving one r-b, ..., r-1 (a = floor(N/2), b = floor((N-1)/2)); each takes one more hop
+      onto rank r, which adds both to its own partial.
+
+    ``out[l]``: fp32 [M/N, ...] per local rank. ``trace`` (a list): transfers carry shard IDs and the
+    list receives (iteration, rank, shard_id) for the ring, (iteration, rank, "A" | "B", shard_id) for
+    unroll-by-2 and (iteration, rank, "left" | "right", shard_id) for bidirectional. ``gate``: the four
+    §5.5 times; when they say the loop does not pay, the original operations run: each rank's whole
+    einsum, then a ReduceScatter of the results.
     """
     n = transport.nranks
     L = transport.local_ranks
     if out[0].dtype != torch.float32:
         raise ValueError("the accumulator (and so the output) of the distributed ReduceScatter is fp32")
+    sched = coco.SCHED_RING if schedule is None else int(schedule)
+    if sched not in (coco.SCHED_RING, coco.SCHED_UNROLL2, coco.SCHED_BIDIRECTIONAL):
+        raise ValueError(f"unknown schedule {schedule!r}")
     md = _dim(spec, "lhs", "m")
     m = lhs[0].shape[md]
     if m % n:
@@ -324,43 +447,106 @@ def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=
     ms = m // n
     if gate is not None and not decompose(gate):
         return _einsum_then_reduce_scatter(spec, lhs, rhs, out, transport, compute)
-    # the accumulator changes buffers at every iteration after the first: start it in the buffer
-    # that makes it end in ``out``
-    other_buf = [torch.empty_like(o) for o in out]
-    acc, inc = (list(out), other_buf) if n % 2 == 1 else (other_buf, list(out))
+    tmode = trace is not None
     part = [torch.empty_like(o) for o in out]
-    ids = nid = None
-    if trace is not None:
-        ids = [torch.zeros((1,), dtype=torch.int64, device=out[0].device) for _ in L]
-        nid = [torch.empty_like(t) for t in ids]
-    for i in range(n):
-        sids = [(q + i + 1) % n for q in L]
-        h = hid = None
-        if i > 0:  # CollectivePermuteStart of the accumulators
-            h = transport.permute(acc, inc)
-            if ids is not None:
-                hid = transport.permute(ids, nid)
-        sl = [x.narrow(md, s * ms, ms) for x, s in zip(lhs, sids)]
-        compute.einsum(spec, sl, list(rhs), acc if i == 0 else part)
+
+    def partial_into(dst, sids):
+        """dst[l] = the partial einsum of local rank l for output shard sids[l] (its LHS rows of it)."""
+        compute.einsum(spec, [x.narrow(md, s_ * ms, ms) for x, s_ in zip(lhs, sids)], list(rhs), dst)
+
+    def step(chain, i, sids, label):
+        """Iteration i of one chain whose transfer (if any) was started: the partial, then the Addition."""
         if i == 0:
-            if ids is not None:
-                for t, s in zip(ids, sids):
-                    t.fill_(s)
+            partial_into(chain.acc, sids)
+            chain.tag(sids)
         else:
-            h.wait()  # CollectivePermuteDone
-            if hid is not None:
-                hid.wait()
-                ids, nid = nid, ids
-            compute.accumulate(inc, part)
-            acc, inc = inc, acc
-        if ids is not None:
-            got = [int(t.item()) for t in ids]
-            if got != sids:
-                raise AssertionError(f"iteration {i}: accumulators {got} in hand, schedule says {sids}")
-            trace.extend((i, q, s) for q, s in zip(L, sids))
-    for a, o in zip(acc, out):  # after N iterations each rank holds its own shard
-        if a.data_ptr() != o.data_ptr():
-            o.copy_(a)
+            partial_into(part, sids)
+            return part
+        return None
+
+    def finish(chain, hs, i, sids, label):
+        if i > 0:
+            chain.done(hs)
+            compute.accumulate(chain.acc, part)
+        chain.check(sids, f"iteration {i}" + (f" ({label})" if label else ""))
+        if tmode:
+            trace.extend(((i, q, s_) if label is None else (i, q, label, s_)) for q, s_ in zip(L, sids))
+
+    if sched == coco.SCHED_RING:
+        # the accumulator changes buffers at every iteration after the first: start it in the buffer that
+        # makes it end in ``out``
+        other_buf = [torch.empty_like(o) for o in out]
+        bufs = (list(out), other_buf) if n % 2 == 1 else (other_buf, list(out))
+        A = _Acc(bufs, 1, transport, tmode)
+        for i in range(n):
+            sids = [(q + i + 1) % n for q in L]
+            hs = A.start() if i > 0 else None
+            step(A, i, sids, None)
+            finish(A, hs, i, sids, None)
+        for x, o in zip(A.acc, out):  # aligned at the loop end: each rank holds its own shard
+            if x.data_ptr() != o.data_ptr():
+                o.copy_(x)
+        return out
+
+    def new(shift):
+        return _Acc(([torch.empty_like(o) for o in out], [torch.empty_like(o) for o in out]), shift, transport,
+                    tmode)
+
+    if sched == coco.SCHED_UNROLL2:
+        na, nb = (n + 1) // 2, n // 2
+        A, B = new(2), new(2)
+        for i in range(na):
+            sa = [(q + 1 + 2 * i) % n for q in L]
+            sb = [(q + 2 + 2 * i) % n for q in L]
+            ha = A.start() if i > 0 else None
+            hb = B.start() if 0 < i < nb else None
+            step(A, i, sa, "A")
+            finish(A, ha, i, sa, "A")
+            if i < nb:
+                step(B, i, sb, "B")
+                finish(B, hb, i, sb, "B")
+        # epilogue: the chain whose last contribution came from rank r+1 takes one more hop
+        if n % 2 == 0:
+            A.shift = 1
+            A.done(A.start())
+        elif n > 1:
+            B.shift = 1
+            B.done(B.start())
+        A.check(list(L), "after the epilogue (A)")
+        if nb:
+            B.check(list(L), "after the epilogue (B)")
+            for l, o in enumerate(out):
+                compute.fused_slice([A.acc[l], B.acc[l]], None, None, 0.0, 0, 0, o)
+        else:
+            for x, o in zip(A.acc, out):
+                o.copy_(x)
+        return out
+
+    # bidirectional
+    a_, b_ = n // 2, (n - 1) // 2
+    left, right = new(1), new(-1)
+    for i in range(max(a_, b_)):
+        sl = [(q + i - a_) % n for q in L]
+        sr = [(q + b_ - i) % n for q in L]
+        hl = left.start() if 0 < i < a_ else None
+        hr = right.start() if 0 < i < b_ else None
+        if i < a_:
+            step(left, i, sl, "left")
+            finish(left, hl, i, sl, "left")
+        if i < b_:
+            step(right, i, sr, "right")
+            finish(right, hr, i, sr, "right")
+    if a_:
+        left.done(left.start())
+        left.check(list(L), "after the epilogue (left)")
+    if b_:
+        right.done(right.start())
+        right.check(list(L), "after the epilogue (right)")
+    partial_into(out, list(L))  # the own partial
+    for l, o in enumerate(out):
+        parts = [o] + ([left.acc[l]] if a_ else []) + ([right.acc[l]] if b_ else [])
+        if len(parts) > 1:
+            compute.fused_slice(parts, None, None, 0.0, 0, 0, o)  # own + left + right, in that order
     return out
 
 

@@ -166,3 +166,64 @@ def test_case3_ring_with_the_looped_operand_on_the_right():
     for a, r, w in zip(out, ref, want):
         assert torch.equal(a, r)
         assert_close(a, w, torch.bfloat16, "ring case 3, looped RHS")
+
+
+@pytest.mark.parametrize("n", [2, 3, 4, 5, 8])
+def test_bidirectional_allgather_einsum_ring(n):
+    """[Decomp] section 5.4.2 with real transfers (loopback): the own shard, then r+k and r-k per step;
+    the same shard order as coco_looped_ag_einsum_sched, so case 1 (DynamicUpdateSlice) is bit-equal
+    and case 2 (Addition, small integers) exact."""
+    m, k, nn = 128, 128, 256
+    shards = [t.to(DEV) for t in synth.per_rank(309, 0, n, (m, k), torch.bfloat16, "smallint")]
+    rhs = [t.to(DEV) for t in synth.per_rank(309, 1, n, (k, nn), torch.bfloat16, "smallint")]
+    out = [torch.empty((n * m, nn), dtype=torch.bfloat16, device=DEV) for _ in range(n)]
+    trace = []
+    ring.looped_allgather_einsum("mk,kn->mn", "lhs", "m", shards, rhs, out, ring.LoopbackTransport(n),
+                                 ring.CocoCompute(), trace, schedule=coco.SCHED_BIDIRECTIONAL)
+    ref = [torch.empty_like(o) for o in out]
+    coco.coco_looped_ag_einsum_sched("mk,kn->mn", coco.sliced(shards, 0), coco.local(rhs), coco.local(ref),
+                                     coco.SCHED_BIDIRECTIONAL)
+    coco.coco_device_status()
+    otrace = []
+    want = oracle.looped_allgather_einsum_bidirectional("mk,kn->mn", "lhs", "m", _f64(shards), _f64(rhs), otrace)
+    for a, b, w in zip(out, ref, want):
+        assert torch.equal(a, b)
+        assert_close(a, w, torch.bfloat16, "bidirectional case 1")
+    assert sorted(trace) == sorted(otrace)
+    # case 2: Addition in the bidirectional order
+    ks = 64
+    shards2 = [t.to(DEV) for t in synth.per_rank(309, 2, n, (m, ks), torch.bfloat16, "smallint")]
+    rhs2 = [t.to(DEV) for t in synth.per_rank(309, 3, n, (n * ks, nn), torch.bfloat16, "smallint")]
+    out2 = [torch.empty((m, nn), dtype=torch.float32, device=DEV) for _ in range(n)]
+    ring.looped_allgather_einsum("mk,kn->mn", "lhs", "k", shards2, rhs2, out2, ring.LoopbackTransport(n),
+                                 ring.CocoCompute(), schedule=coco.SCHED_BIDIRECTIONAL)
+    want2 = oracle.looped_allgather_einsum_bidirectional("mk,kn->mn", "lhs", "k", _f64(shards2), _f64(rhs2))
+    torch.cuda.synchronize()
+    for a, w in zip(out2, want2):
+        assert np.array_equal(synth.as_f64(a), w)
+
+
+@pytest.mark.parametrize("sched", [1, 2])
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 8])
+def test_reduce_scatter_ring_schedules(sched, n):
+    """Unroll-by-2 (section 5.4.1) and bidirectional (section 5.4.2) Einsum-ReduceScatter with real
+    transfers (loopback): small-integer inputs, so every sum is exact and equal to the single-launch
+    schedule's and the oracle's."""
+    ms, k, nn = 128, 128, 256
+    lhs = [t.to(DEV) for t in synth.per_rank(310, 0, n, (n * ms, k), torch.bfloat16, "smallint")]
+    rhs = [t.to(DEV) for t in synth.per_rank(310, 1, n, (k, nn), torch.bfloat16, "smallint")]
+    out = [torch.empty((ms, nn), dtype=torch.float32, device=DEV) for _ in range(n)]
+    trace = []
+    ring.looped_einsum_reduce_scatter("mk,kn->mn", lhs, rhs, out, ring.LoopbackTransport(n), ring.CocoCompute(),
+                                      trace, schedule=sched)
+    ref = [torch.empty_like(o) for o in out]
+    coco.coco_looped_einsum_rs_sched("mk,kn->mn", coco.sliced(lhs, 1), coco.sliced(rhs, 0), coco.sliced(ref, 0),
+                                     sched)
+    coco.coco_device_status()
+    fn = oracle.looped_einsum_reduce_scatter_unrolled if sched == 1 else oracle.looped_einsum_reduce_scatter_bidirectional
+    otrace = []
+    want = fn("mk,kn->mn", _f64(lhs), _f64(rhs), "m", otrace)
+    for a, b, w in zip(out, ref, want):
+        assert torch.equal(a, b)
+        assert np.array_equal(synth.as_f64(a), w)
+    assert sorted(trace) == sorted(otrace)

@@ -1,5 +1,5 @@
 """The one-rank-per-process Looped CollectiveEinsum and FusedAllReduce
-(``collective_fusedallreduce_gb300.ring``) on CPU: gloo, world sizes 2 and 3.
+(``collective_fusedallreduce_gb300.ring``) on CPU: gloo, world sizes 2, 3 and 4.
 
 Each rank is a process that owns only its own shards; every CollectivePermute,
 all-to-all and all-gather goes through torch.distributed. The steps'
@@ -12,7 +12,8 @@ permute direction and double buffers, the shard IDs that travel with the data
 DynamicUpdateSlice offsets, the order of the ReduceScatter's additions, the
 FusedAllReduce's slices and element indices, and the §5.5 gate's fallback.
 World size 3 tells the permute direction apart ({j -> j-1} and {j -> j+1}
-coincide for 2 ranks).
+coincide for 2 ranks); world size 4 takes the even-N ends of the bidirectional
+and unroll-by-2 schedules.
 """
 
 import os
@@ -135,6 +136,28 @@ def _run(rank, world, port, q):
         ring.looped_einsum_reduce_scatter("mk,kn->mn", [x["rs_lhs"][rank]], [x["rs_rhs"][rank]], kept, T, C, gate=keep)
         res["rs_gated"] = (bool(np.array_equal(f64(kept[0]), want)), True)
 
+        # the section 5.4 schedules: bidirectional AllGather-Einsum (cases 1, 2, 3), unroll-by-2 and
+        # bidirectional Einsum-ReduceScatter, each against the oracle's restatement and its shard IDs
+        for key, spec, lab, shape in (("c1", "mk,kn->mn", "m", (4 * world, 6)), ("c2", "mk,kn->mn", "k", (4, 5)),
+                                      ("c3", "bmk,bkn->bmn", "b", (2 * world, 3, 5))):
+            trace, otrace = [], []
+            out = [torch.zeros(shape)]
+            ring.looped_allgather_einsum(spec, "lhs", lab, [x[key + "_shards"][rank]], [x[key + "_rhs"][rank]], out,
+                                         T, C, trace=trace, schedule=2)
+            want = oracle.looped_allgather_einsum_bidirectional(spec, "lhs", lab, [f64(v) for v in x[key + "_shards"]],
+                                                                [f64(v) for v in x[key + "_rhs"]], otrace)[rank]
+            res[key + "_bidirectional"] = (bool(np.array_equal(f64(out[0]), want)),
+                                           sorted(trace) == sorted(t for t in otrace if t[1] == rank))
+        for sched, fn in ((1, oracle.looped_einsum_reduce_scatter_unrolled),
+                          (2, oracle.looped_einsum_reduce_scatter_bidirectional)):
+            trace, otrace = [], []
+            out = [torch.zeros((2, 4))]
+            ring.looped_einsum_reduce_scatter("mk,kn->mn", [x["rs_lhs"][rank]], [x["rs_rhs"][rank]], out, T, C,
+                                              trace, schedule=sched)
+            want = fn("mk,kn->mn", [f64(v) for v in x["rs_lhs"]], [f64(v) for v in x["rs_rhs"]], "m", otrace)[rank]
+            res[f"rs_sched{sched}"] = (bool(np.array_equal(f64(out[0]), want)),
+                                       sorted(trace) == sorted(t for t in otrace if t[1] == rank))
+
         out = [torch.empty((2 * world, 16))]
         ring.fused_allreduce([x["far_partials"][rank]], x["far_bias"], [x["far_res"]], 0.25, 1234, out, T, C)
         want = oracle.fused_allreduce([f64(p) for p in x["far_partials"]], f64(x["far_bias"]), f64(x["far_res"]),
@@ -156,7 +179,7 @@ def _free_port():
     return p
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 4])
 def test_ring_over_gloo_matches_the_oracle(world):
     import __graft_entry__
     __graft_entry__.build()  # the schedule comes from the library (host-only calls)
