@@ -12,6 +12,9 @@ owns its buffers and the data really moves:
   transfer runs, then waiting for it (CollectivePermuteDone). AllGather-
   Einsum: cases 1, 2 and 3 of §5.1; Einsum-ReduceScatter: the accumulator
   travels and each rank adds its partial for the shard ID it receives.
+* [Decomp] §5.4: the bidirectional AllGather-Einsum and the unroll-by-2 and
+  bidirectional Einsum-ReduceScatter, with their chains travelling in both
+  directions or two hops at a time.
 * [Decomp] §5.5: the loop replaces the original collective + einsum only when
   the cost model says it pays (coco_loop_profitable); otherwise the original
   operations run (AllGather then one einsum, or the einsum then a
@@ -455,14 +458,13 @@ def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=
         compute.einsum(spec, [x.narrow(md, s_ * ms, ms) for x, s_ in zip(lhs, sids)], list(rhs), dst)
 
     def step(chain, i, sids, label):
-        """Iteration i of one chain whose transfer (if any) was started: the partial, then the Addition."""
+        """Iteration i of one chain whose transfer (if any) was started: its partial einsum (the first one
+        straight into the accumulator, later ones into ``part`` for the Addition in finish)."""
         if i == 0:
             partial_into(chain.acc, sids)
             chain.tag(sids)
         else:
             partial_into(part, sids)
-            return part
-        return None
 
     def finish(chain, hs, i, sids, label):
         if i > 0:
