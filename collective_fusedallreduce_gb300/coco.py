@@ -79,6 +79,7 @@ for _name, _args in {
     "coco_allreduce_rs_ag": [_P, _P, _P, _S],
     "coco_allreduce_rs_ag_noalloc": [_P, _P, _S],
     "coco_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
+    "coco_einsum_accumulate": [ctypes.c_char_p, _P, _P, _P, _S],
     "coco_matmul_fused_allreduce": [ctypes.c_char_p, _P, _P, ctypes.c_void_p, _P, ctypes.c_float, ctypes.c_uint64,
                                     _P, _S],
     "coco_looped_ag_einsum": [ctypes.c_char_p, _P, _P, _P, _S],
@@ -119,7 +120,7 @@ _lib.coco_plan_cache_clear.restype = None
 EXPORTED = [
     "coco_fused_allreduce", "coco_fused_allreduce_at", "coco_allreduce", "coco_reduce_scatter", "coco_allgather", "coco_allreduce_rs_ag",
     "coco_allreduce_rs_ag_noalloc",
-    "coco_einsum", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs",
+    "coco_einsum", "coco_einsum_accumulate", "coco_matmul_fused_allreduce", "coco_looped_ag_einsum", "coco_looped_einsum_rs",
     "coco_looped_ag_einsum_sched", "coco_looped_einsum_rs_sched", "coco_dropout_keep_mask",
     "coco_scattered_table_bytes", "coco_scattered_table_build", "coco_scattered_allreduce",
     "coco_device_status", "coco_wait_selftest", "coco_kernel_launches", "coco_last_cuda_error", "coco_status_string", "coco_version",
@@ -242,6 +243,11 @@ def coco_allreduce_rs_ag_noalloc(inp, out, stream=None):
 
 def coco_einsum(spec, lhs, rhs, out, stream=None):
     _check(_lib.coco_einsum(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), _stream(stream)), "coco_einsum")
+
+
+def coco_einsum_accumulate(spec, lhs, rhs, out, stream=None):
+    _check(_lib.coco_einsum_accumulate(spec.encode(), _ref(lhs), _ref(rhs), _ref(out), _stream(stream)),
+           "coco_einsum_accumulate")
 
 
 def coco_matmul_fused_allreduce(spec, lhs, rhs, bias, residual, dropout_p, seed, out, stream=None):

@@ -853,6 +853,47 @@ COCO_EXPORT coco_status coco_einsum(const char* spec, const coco_tensor* lhs, co
   return finish(P, E, a.c, key, stream);
 }
 
+COCO_EXPORT coco_status coco_einsum_accumulate(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                               const coco_tensor* out, void* stream) {
+  PlanKey key(5);
+  key.str(spec);
+  key.tensor(lhs);
+  key.tensor(rhs);
+  key.tensor(out);
+  coco_status cst;
+  if (run_cached(key, stream, &cst)) return cst;
+  EinsumArgs E;
+  coco_status st = check_einsum_common(spec, lhs, rhs, out, &E);
+  if (st != COCO_OK) return st;
+  const Spec& S = E.spec;
+  const int kl = S.batched ? 2 : 1, kr = S.batched ? 1 : 0;
+  if (E.lhs.layout == COCO_REPLICATED) return COCO_ERR_LAYOUT;
+  if (E.lhs.layout == COCO_SLICED && E.lhs.slice_dim != kl) return COCO_ERR_LAYOUT;
+  if (E.rhs.layout == COCO_SLICED && E.rhs.slice_dim != kr) return COCO_ERR_LAYOUT;
+  if (E.out.layout != COCO_LOCAL) return COCO_ERR_LAYOUT;
+  if (E.out.dtype != COCO_F32) return COCO_ERR_DTYPE;
+  const Dims3 a = dims_of(S, E.lhs.local), b = dims_of(S, E.rhs.local), o = dims_of(S, E.out.local);
+  if (a.c != b.r || a.b != b.b || o.b != a.b || o.r != a.r || o.c != b.c) return COCO_ERR_SHAPE;
+  if (E.out.numel == 0) return COCO_OK;
+  if ((st = einsum_alias(E.lhs, E.rhs, E.out)) != COCO_OK) return st;
+  if (a.c == 0) return COCO_OK;  // adds nothing
+  GemmPlan P;
+  P.mode = EPI_ADD;
+  P.in_dtype = E.lhs.dtype;
+  P.out_dtype = COCO_F32;
+  for (int g = 0; g < E.out.ngroups; ++g)
+    for (int r = 0; r < E.out.nranks; ++r) {
+      Job J = make_job(add_out(&P, make_out(E.out.ptr(g, r), o)), o);
+      J.res = E.out.ptr(g, r);  // the addend is the output itself, read before it is written
+      J.seg0 = static_cast<int16_t>(P.segs.size());
+      J.nseg = 1;
+      P.segs.push_back(make_seg(add_view(&P, make_view(E.lhs.ptr(g, r), a)),
+                                add_view(&P, make_view(operand_ptr(E.rhs, g, r), b)), a.c));
+      P.jobs.push_back(J);
+    }
+  return run_keyed(std::move(P), key, static_cast<cudaStream_t>(stream));
+}
+
 COCO_EXPORT coco_status coco_matmul_fused_allreduce(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
                                                     const void* bias, const coco_tensor* residual, float dropout_p,
                                                     uint64_t seed, const coco_tensor* out, void* stream) {

@@ -29,6 +29,7 @@ struct SimtParams {
   OutView outs[MAX_OUTS];
   int32_t tile_start[MAX_JOBS + 1];
   int32_t njobs, total_tiles, out_dtype;
+  int32_t accumulate;  // EPI_ADD: out (fp32) += the product
 };
 static_assert(sizeof(SimtParams) <= 32000, "kernel parameter block too large");
 
@@ -91,7 +92,10 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const __grid_constant__ SimtP
         if (col >= J.n) continue;
         const int64_t off = static_cast<int64_t>(J.o_b0 + bb) * O.bstride + static_cast<int64_t>(J.o_r0 + row) * O.ld +
                             (J.o_c0 + col);
-        if (P.out_dtype == COCO_F32) static_cast<float*>(O.ptr)[off] = acc[i][q];
+        if (P.out_dtype == COCO_F32) {
+          float* o = static_cast<float*>(O.ptr) + off;
+          *o = P.accumulate ? *o + acc[i][q] : acc[i][q];
+        }
         else if (P.out_dtype == COCO_F16) static_cast<__half*>(O.ptr)[off] = __float2half_rn(acc[i][q]);
         else static_cast<__nv_bfloat16*>(O.ptr)[off] = __float2bfloat16_rn(acc[i][q]);
       }
@@ -142,6 +146,7 @@ cudaError_t launch_gemm_simt(const GemmPlan& plan, cudaStream_t s) {
     P->njobs = njobs;
     P->total_tiles = tiles;
     P->out_dtype = plan.out_dtype;
+    P->accumulate = plan.mode == EPI_ADD ? 1 : 0;
     const int cap = sm_count() * 4;
     k_gemm_simt<<<tiles < cap ? tiles : cap, 256, 0, s>>>(*P);
     count_launch();

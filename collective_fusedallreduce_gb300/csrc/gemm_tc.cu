@@ -109,7 +109,7 @@ struct TcParams {
   uint32_t idesc;
   int32_t out_dtype;
   unsigned int* err;
-  // FusedAllReduce epilogue (EPI_FUSED_ALLREDUCE only)
+  // FusedAllReduce epilogue (EPI_FUSED_ALLREDUCE only; EPI_ADD uses none of it)
   const void* bias;
   uint64_t seed;
   uint32_t keep_threshold;
@@ -435,7 +435,10 @@ __device__ __forceinline__ bool keep_state(uint64_t z, uint32_t threshold) {
 // accumulator is a sum over ranks (the K-segments are the ranks' K-slices);
 // add the bias, apply dropout and add the residual in registers, then store
 // the tile to every replica of the group ([CoCoNet] §5.2, FusedAllReduce,
-// with the MatMul of its Fig. 3 fused in front).
+// with the MatMul of its Fig. 3 fused in front). MODE = EPI_ADD: add the
+// output's present values (fp32) to the accumulator and store the sum in
+// place ([Decomp] §5.1's Addition fused into the partial einsum, as its §5.4.1
+// describes the loop's accumulation).
 template <int MODE, bool TWO_SM>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::THREADS, 1)
     k_gemm_tc(const __grid_constant__ TcParams P) {
@@ -475,7 +478,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       mbar_init(tempty_bar(a), (TWO_SM ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
-    if constexpr (MODE == EPI_FUSED_ALLREDUCE)
+    if constexpr (MODE != EPI_STORE)
       for (int w = 0; w < EPI_WARPS; ++w) mbar_init(bar0 + 8u * (2 * STAGES + 5 + w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -693,7 +696,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       const int acc = local & 1;
       const uint32_t aph = (local >> 1) & 1;
       const int row0 = T.mt * BM + quarter * 32;  // job-relative row of this warp's lane 0
-      const bool has_res = MODE == EPI_FUSED_ALLREDUCE && J.res != nullptr;
+      const bool has_res = MODE != EPI_STORE && J.res != nullptr;
       auto load_residual = [&](int cc) {  // lane 0 only
         mbar_expect_tx(res_bar, EPI_STRIP);
         tma_load_3d(res_strip, &P.omaps[J.res_map], res_bar, J.o_c0 + T.nt * BN + cc, J.o_r0 + row0,
@@ -705,11 +708,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       // the bias, lane l holding tile columns [8l, 8l + 8) for the lanes that
       // need them (shuffles), instead of one dependent global load per column group.
       uint4 bias_v = make_uint4(0u, 0u, 0u, 0u);
-      if constexpr (MODE == EPI_FUSED_ALLREDUCE) {
+      if constexpr (MODE != EPI_STORE) {
         if (has_res && lane == 0) {
           load_residual(col_begin);
           res_pending = true;
         }
+      }
+      if constexpr (MODE == EPI_FUSED_ALLREDUCE) {
         const int bc = J.o_c0 + T.nt * BN + 8 * lane;
         if (bias_ptr && bc < O.cols) bias_v = ld_nc_v4(bias_ptr + bc * 2);
       }
@@ -731,7 +736,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
       for (int c0 = col_begin; c0 < col_begin + COLS; c0 += cols_per_chunk) {
         const bool last = c0 + cols_per_chunk >= col_begin + COLS;
         uint32_t p[32];
-        if constexpr (MODE == EPI_FUSED_ALLREDUCE) {
+        if constexpr (MODE == EPI_ADD) {
+          // fp32 output: 32 columns of this lane's row, plus the same columns of the output as they were
+          // (the addend strip, loaded by TMA one chunk ahead)
+          uint4 cur[8];
+          const bool landed = __all_sync(0xffffffffu, mbar_wait(res_bar, res_phase, abort_flag));
+          if (!landed) {
+            if (lane == 0) fail();
+            break;
+          }
+          res_phase ^= 1u;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) cur[c] = ld_shared_v4(res_strip + lane * 128 + ((c ^ (lane & 7)) << 4));
+          fence_proxy_async_smem();  // these reads come before the next TMA write of the strip
+          __syncwarp();
+          if (lane == 0) {
+            res_pending = !last;
+            if (!last) load_residual(c0 + cols_per_chunk);
+          }
+          uint32_t r[32];
+          tmem_ld32(tbase + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            p[4 * c + 0] = __float_as_uint(__uint_as_float(cur[c].x) + __uint_as_float(r[4 * c + 0]));
+            p[4 * c + 1] = __float_as_uint(__uint_as_float(cur[c].y) + __uint_as_float(r[4 * c + 1]));
+            p[4 * c + 2] = __float_as_uint(__uint_as_float(cur[c].z) + __uint_as_float(r[4 * c + 2]));
+            p[4 * c + 3] = __float_as_uint(__uint_as_float(cur[c].w) + __uint_as_float(r[4 * c + 3]));
+          }
+        } else if constexpr (MODE == EPI_FUSED_ALLREDUCE) {
           // 16-bit output: 64 columns of this lane's row
           const int gcol0 = J.o_c0 + T.nt * BN + c0;
           uint4 cur[8];
@@ -808,11 +841,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE, TWO_SM>::T
         // commit no bulk group, so after a bulk-stored tile the group count no longer tells which
         // strip is free: such chunks wait for every earlier bulk store to have read its strip.
         if (lane == 0) {
-          if (MODE == EPI_FUSED_ALLREDUCE || !bulk) bulk_wait_read_all();
+          if (MODE != EPI_STORE || !bulk) bulk_wait_read_all();
           else bulk_wait_read_le1();
         }
         __syncwarp();
-        const uint32_t strip = MODE == EPI_FUSED_ALLREDUCE ? strips : strips + buf * EPI_STRIP;
+        const uint32_t strip = MODE != EPI_STORE ? strips : strips + buf * EPI_STRIP;
 #pragma unroll
         for (int c = 0; c < 8; ++c)  // row = lane, 16-byte chunk c at its 128-byte-swizzle slot
           st_shared_v4(strip + lane * 128 + ((c ^ (lane & 7)) << 4), p[4 * c], p[4 * c + 1], p[4 * c + 2],
@@ -1314,7 +1347,7 @@ bool encode_out(CUtensorMap* map, const OutView& o, int dtype) {
 
 // per kernel variant and device: the dynamic shared-memory limit was raised (static storage: starts false;
 // atomic because calls may come from several host threads, which at worst both set the attribute)
-std::atomic<bool> smem_configured[5][64];
+std::atomic<bool> smem_configured[7][64];
 
 }  // namespace
 
@@ -1351,7 +1384,9 @@ cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out) {
   *out = nullptr;
   if (!encode_fn()) return cudaErrorNotSupported;
   const bool far = plan.mode == EPI_FUSED_ALLREDUCE;
+  const bool add = plan.mode == EPI_ADD;
   if (far && plan.out_dtype == COCO_F32) return cudaErrorNotSupported;
+  if (add && plan.out_dtype != COCO_F32) return cudaErrorNotSupported;
   // Every job (one output region's whole K-segment loop) must fit one launch's parameter block:
   // checked for all jobs before anything is launched, so an unsupported plan runs nothing.
   for (const Job& J : plan.jobs) {
@@ -1362,7 +1397,7 @@ cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out) {
       if (std::find(bs.begin(), bs.end(), S.b) == bs.end()) bs.push_back(S.b);
     }
     if (static_cast<int>(as.size() + bs.size()) > MAX_MAPS || J.nseg > MAX_SEGS ||
-        J.nout + (far && J.res ? 1 : 0) > MAX_OUTS)
+        J.nout + ((far || add) && J.res ? 1 : 0) > MAX_OUTS)
       return cudaErrorNotSupported;
   }
   // k-blocks per tile, averaged over the plan's jobs
@@ -1371,13 +1406,13 @@ cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out) {
     for (int k = 0; k < J.nseg; ++k) kb_sum += (plan.segs[J.seg0 + k].klen + BK - 1) / BK;
   const bool two_sm = plan.jobs.empty() ? true : kb_sum >= static_cast<int64_t>(kTwoSmMinKBlocks) * plan.jobs.size();
   // jobs of at most BS_KB k-blocks are store-bound: the B-stationary kernel halves their operand loads
-  bool bs = !far && !plan.jobs.empty();
+  bool bs = plan.mode == EPI_STORE && !plan.jobs.empty();
   for (const Job& J : plan.jobs) {
     int kb = 0;
     for (int k = 0; k < J.nseg; ++k) kb += (plan.segs[J.seg0 + k].klen + BK - 1) / BK;
     bs = bs && kb <= BS_KB;
   }
-  const int variant = bs ? 4 : (far ? 2 : 0) + (two_sm ? 1 : 0);
+  const int variant = bs ? 4 : (add ? 5 : far ? 2 : 0) + (two_sm ? 1 : 0);
   void (*kernel)(TcParams) = nullptr;
   int smem = 0, threads = 0;
   switch (variant) {
@@ -1388,8 +1423,12 @@ cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out) {
             threads = Cfg<EPI_STORE, true>::THREADS; break;
     case 2: kernel = k_gemm_tc<EPI_FUSED_ALLREDUCE, false>; smem = Cfg<EPI_FUSED_ALLREDUCE, false>::SMEM_BYTES;
             threads = Cfg<EPI_FUSED_ALLREDUCE, false>::THREADS; break;
-    default: kernel = k_gemm_tc<EPI_FUSED_ALLREDUCE, true>; smem = Cfg<EPI_FUSED_ALLREDUCE, true>::SMEM_BYTES;
-             threads = Cfg<EPI_FUSED_ALLREDUCE, true>::THREADS; break;
+    case 3: kernel = k_gemm_tc<EPI_FUSED_ALLREDUCE, true>; smem = Cfg<EPI_FUSED_ALLREDUCE, true>::SMEM_BYTES;
+            threads = Cfg<EPI_FUSED_ALLREDUCE, true>::THREADS; break;
+    case 5: kernel = k_gemm_tc<EPI_ADD, false>; smem = Cfg<EPI_ADD, false>::SMEM_BYTES;
+            threads = Cfg<EPI_ADD, false>::THREADS; break;
+    default: kernel = k_gemm_tc<EPI_ADD, true>; smem = Cfg<EPI_ADD, true>::SMEM_BYTES;
+             threads = Cfg<EPI_ADD, true>::THREADS; break;
   }
   int dev = 0;
   cudaGetDevice(&dev);
@@ -1432,7 +1471,7 @@ cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out) {
       int found = -1;
       for (size_t q = 0; q < orange.size(); ++q)
         if (orange[q].first == J.out && orange[q].second == J.nout) found = obase[q];
-      const int need_out = (found < 0 ? J.nout : 0) + (far && J.res ? 1 : 0);
+      const int need_out = (found < 0 ? J.nout : 0) + ((far || add) && J.res ? 1 : 0);
       if (nmaps + need_maps > MAX_MAPS || nsegs + J.nseg > MAX_SEGS || nouts + need_out > MAX_OUTS) break;
       Job nj = J;
       nj.seg0 = static_cast<int16_t>(nsegs);
@@ -1464,7 +1503,7 @@ cudaError_t tc_prepare(const GemmPlan& plan, TcPrepared** out) {
       }
       nj.out = found;
       nj.res_map = -1;
-      if (far && J.res) {  // the residual has the output's shape: a map like the outputs' (box 32 rows)
+      if ((far || add) && J.res) {  // the residual / addend has the output's shape: a map like the outputs'
         OutView rv = plan.outs[J.out];
         rv.ptr = const_cast<void*>(J.res);
         if (!encode_out(&P->omaps[nouts], rv, plan.out_dtype)) { status = cudaErrorInvalidValue; break; }

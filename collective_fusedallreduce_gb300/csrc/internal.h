@@ -107,7 +107,9 @@ struct Job {
 };
 
 // The epilogue applied to every accumulator tile.
-enum EpilogueMode { EPI_STORE = 0, EPI_FUSED_ALLREDUCE = 1 };
+// EPI_ADD: out = out + accumulator, fp32 output (the Addition of the Looped CollectiveEinsum fused into
+// the einsum); the job's `res` is its own output, read one strip ahead like the residual.
+enum EpilogueMode { EPI_STORE = 0, EPI_FUSED_ALLREDUCE = 1, EPI_ADD = 2 };
 
 // Pointwise part of the FusedAllReduce epilogue (bias over the last
 // dimension, counter-hash dropout, then the residual), as in coco_fused_allreduce.

@@ -159,6 +159,11 @@ class CocoCompute:
         self._cuda(lhs + rhs + out)
         coco.coco_einsum(spec, coco.local(lhs), coco.local(rhs), coco.local(out), self.stream)
 
+    def einsum_accumulate(self, spec, lhs, rhs, acc):
+        """acc[l] += lhs[l] @ rhs[l] (fp32), the Addition done in the einsum's epilogue (one launch)."""
+        self._cuda(lhs + rhs + acc)
+        coco.coco_einsum_accumulate(spec, coco.local(lhs), coco.local(rhs), coco.local(acc), self.stream)
+
     def accumulate(self, acc, part):
         """acc[l] = acc[l] + part[l] in the accumulator's type (one launch: a two-rank sum per local rank)."""
         self._cuda(acc + part)
@@ -280,7 +285,6 @@ def looped_allgather_einsum(spec, looped, slice_label, shard, other, out, transp
     if gate is not None and not decompose(gate):
         return _allgather_then_einsum(spec, looped, sd, shard, other, out, transport, compute)
 
-    scratch = []
     used = [0]  # partial einsums done (case 2: the first one writes out, the others add)
 
     def partial(held, sids, step):
@@ -295,11 +299,8 @@ def looped_allgather_einsum(spec, looped, slice_label, shard, other, out, transp
             lhs, rhs = (held, oth) if looped == "lhs" else (oth, held)
             if used[0] == 0:
                 compute.einsum(spec, lhs, rhs, out)
-            else:
-                if not scratch:
-                    scratch.extend(torch.empty_like(o) for o in out)
-                compute.einsum(spec, lhs, rhs, scratch)
-                compute.accumulate(out, scratch)
+            else:  # the Addition fused into the partial einsum (the shard in hand is not in flight)
+                compute.einsum_accumulate(spec, lhs, rhs, out)
         else:
             od = spec.replace(" ", "").split("->")[1].index(slice_label)
             dst = [o.narrow(od, sid * ext, ext) for o, sid in zip(out, sids)]
@@ -424,8 +425,11 @@ def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=
     * coco.SCHED_RING (default): one accumulator {j -> j-1}; at iteration i rank q adds its partial for
       shard (q+i+1) mod N; output shard r collects the ranks r-1, r-2, ..., r.
     * coco.SCHED_UNROLL2 ([Decomp] §5.4.1): two interleaved chains travelling two hops per iteration,
-      chain A collecting ranks r-1, r-3, ... and chain B ranks r-2, r-4, ...; the chain that ends one
-      hop short takes one more hop and rank r adds the two.
+      chain A collecting ranks r-1, r-3, ... and chain B ranks r-2, r-4, ...; each chain's Addition is
+      fused into its partial einsum (coco_einsum_accumulate) and runs while the other chain travels; the
+      chain that ends one hop short takes one more hop and rank r adds the two.
+    The ring and bidirectional forms compute each partial while its accumulator is in flight and add
+    it once the accumulator has arrived (the fused form would have to wait for the transfer first).
     * coco.SCHED_BIDIRECTIONAL ([Decomp] §5.4.2): a left-moving accumulator collects ranks r+a, ..., r+1
       and a right-moving one r-b, ..., r-1 (a = floor(N/2), b = floor((N-1)/2)); each takes one more hop
       onto rank r, which adds both to its own partial.
@@ -495,18 +499,39 @@ def looped_einsum_reduce_scatter(spec, lhs, rhs, out, transport, compute, trace=
                     tmode)
 
     if sched == coco.SCHED_UNROLL2:
+        # The two chains alternate so that each one's Addition, fused into its partial einsum (which needs
+        # the accumulator to have arrived), runs while the other chain's accumulator is in flight: the
+        # point of unrolling by 2 in [Decomp] §5.4.1.
         na, nb = (n + 1) // 2, n // 2
         A, B = new(2), new(2)
-        for i in range(na):
-            sa = [(q + 1 + 2 * i) % n for q in L]
-            sb = [(q + 2 + 2 * i) % n for q in L]
-            ha = A.start() if i > 0 else None
-            hb = B.start() if 0 < i < nb else None
-            step(A, i, sa, "A")
-            finish(A, ha, i, sa, "A")
+
+        def fused(chain, i, sids, label):
+            compute.einsum_accumulate(spec, [x.narrow(md, s_ * ms, ms) for x, s_ in zip(lhs, sids)], list(rhs),
+                                      chain.acc)
+            chain.check(sids, f"iteration {i} ({label})")
+            if tmode:
+                trace.extend((i, q, label, s_) for q, s_ in zip(L, sids))
+
+        def sids_a(i):
+            return [(q + 1 + 2 * i) % n for q in L]
+
+        def sids_b(i):
+            return [(q + 2 + 2 * i) % n for q in L]
+
+        step(A, 0, sids_a(0), "A")
+        finish(A, None, 0, sids_a(0), "A")
+        ha = A.start() if na > 1 else None
+        if nb:
+            step(B, 0, sids_b(0), "B")
+            finish(B, None, 0, sids_b(0), "B")
+        for i in range(1, na):
+            A.done(ha)
+            hb = B.start() if i < nb else None
+            fused(A, i, sids_a(i), "A")  # while B travels
+            ha = A.start() if i + 1 < na else None
             if i < nb:
-                step(B, i, sb, "B")
-                finish(B, hb, i, sb, "B")
+                B.done(hb)
+                fused(B, i, sids_b(i), "B")  # while A travels
         # epilogue: the chain whose last contribution came from rank r+1 takes one more hop
         if n % 2 == 0:
             A.shift = 1

@@ -288,6 +288,18 @@ coco_status coco_einsum(const char* spec, const coco_tensor* lhs, const coco_ten
                         const coco_tensor* out, void* stream);
 
 /*
+ * out_r += lhs_r @ rhs_r for every rank r, with the addition done in the einsum's epilogue: each output
+ * element is read once, added to the fp32 accumulator and written once (the Addition update of the
+ * Looped CollectiveEinsum fused into the partial einsum, [Decomp] §5.1 and the loop of §5.4.1; used by
+ * the one-rank-per-device loops, where an accumulator or a case-2 output grows by one partial each
+ * iteration). Operands as coco_einsum; `out` is LOCAL, fp32 (else COCO_ERR_DTYPE), read and written in
+ * place, and may not overlap an operand (COCO_ERR_ALIAS). A contraction of length 0 leaves `out` as it
+ * is. fp32 operands run on the FMA path.
+ */
+coco_status coco_einsum_accumulate(const char* spec, const coco_tensor* lhs, const coco_tensor* rhs,
+                                   const coco_tensor* out, void* stream);
+
+/*
  * MatMul fused with FusedAllReduce ([CoCoNet] Fig. 3 lines 7-13; the
  * overlap of its MatMul with the AllReduce, §5.3 / Fig. 9, taken to a single
  * kernel on one GPU):
@@ -440,7 +452,7 @@ coco_status coco_wait_selftest(uint64_t timeout_ns, void* stream);
 uint64_t coco_kernel_launches(void);
 
 /*
- * Plan cache of the einsum entry points (coco_einsum, coco_matmul_fused_allreduce,
+ * Plan cache of the einsum entry points (coco_einsum, coco_einsum_accumulate, coco_matmul_fused_allreduce,
  * coco_looped_ag_einsum[_sched], coco_looped_einsum_rs[_sched]). A call whose
  * arguments repeat an earlier valid call's exactly (entry point, spec,
  * schedule, every in-use field of every coco_tensor including its pointers,

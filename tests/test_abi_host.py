@@ -452,3 +452,19 @@ def test_plan_cache_under_concurrent_calls(coco):
     h1, m1, e1 = coco.coco_plan_cache_stats()
     assert (h1 - h0) + (m1 - m0) == 401 and e1 >= 3
     coco.coco_plan_cache_clear()
+
+
+def test_einsum_accumulate_validation(coco):
+    B16, L = coco.BF16, coco.LOCAL
+    lhs = mk(coco, B16, L, (64, 32), 4)
+    rhs = mk(coco, B16, L, (32, 16), 4, base=FAKE + (1 << 40))
+    A = "coco_einsum_accumulate"
+    assert ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, B16, L, (64, 16), 4, base=FAKE + (1 << 41))) == 3  # not fp32
+    assert ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, coco.F32, coco.REPLICATED, (64, 16), 4,
+                                                   base=FAKE + (1 << 41))) == 4
+    assert ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, coco.F32, L, (64, 24), 4, base=FAKE + (1 << 41))) == 2
+    assert ein(coco, A, b"mk,kn->mn", lhs, rhs, mk(coco, coco.F32, L, (64, 16), 4, base=FAKE + (1 << 40))) == 6
+    empty_k = mk(coco, B16, L, (64, 0), 4)
+    # zero contraction: nothing to add, no CUDA call
+    assert ein(coco, A, b"mk,kn->mn", empty_k, mk(coco, B16, L, (0, 16), 4, base=FAKE + (1 << 40)),
+               mk(coco, coco.F32, L, (64, 16), 4, base=FAKE + (1 << 41))) == 0

@@ -44,6 +44,11 @@ class NumpyCompute:
         for a, b, o in zip(lhs, rhs, out):
             self._store(o, oracle.einsum(spec, self._f64(a), self._f64(b)))
 
+    def einsum_accumulate(self, spec, lhs, rhs, acc):
+        import oracle
+        for a, b, c in zip(lhs, rhs, acc):
+            self._store(c, self._f64(c) + oracle.einsum(spec, self._f64(a), self._f64(b)))
+
     def accumulate(self, acc, part):
         for a, p in zip(acc, part):
             self._store(a, self._f64(a) + self._f64(p))
