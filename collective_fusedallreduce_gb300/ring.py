@@ -143,7 +143,13 @@ class LoopbackTransport:
 
 
 class CocoCompute:
-    """The steps' arithmetic through the library's kernels (CUDA tensors only)."""
+    """The steps' arithmetic through the library's kernels (CUDA tensors only).
+
+    ``stream``: the CUDA stream the kernels are enqueued on; by default the current stream at each call.
+    torch.distributed orders its transfers against the current stream (a transfer starts after the work
+    enqueued there, and wait() makes the current stream wait for it), so a different stream is joined to
+    the current one around every call: it waits for the current stream's work first, and the current
+    stream waits for its kernels afterwards."""
 
     def __init__(self, stream=None):
         self.stream = stream
@@ -154,15 +160,25 @@ class CocoCompute:
             if not t.is_cuda:
                 raise RuntimeError("CocoCompute runs the library's CUDA kernels: tensors must be on a GPU")
 
+    def _launch(self, fn, *args):
+        s = self.stream
+        cur = None if s is None else torch.cuda.current_stream(s.device)
+        joined = cur is not None and cur != s
+        if joined:
+            s.wait_stream(cur)
+        fn(*args, s)
+        if joined:
+            cur.wait_stream(s)
+
     def einsum(self, spec, lhs, rhs, out):
         """out[l] = lhs[l] @ rhs[l] for every local rank l (one launch)."""
         self._cuda(lhs + rhs + out)
-        coco.coco_einsum(spec, coco.local(lhs), coco.local(rhs), coco.local(out), self.stream)
+        self._launch(coco.coco_einsum, spec, coco.local(lhs), coco.local(rhs), coco.local(out))
 
     def einsum_accumulate(self, spec, lhs, rhs, acc):
         """acc[l] += lhs[l] @ rhs[l] (fp32), the Addition done in the einsum's epilogue (one launch)."""
         self._cuda(lhs + rhs + acc)
-        coco.coco_einsum_accumulate(spec, coco.local(lhs), coco.local(rhs), coco.local(acc), self.stream)
+        self._launch(coco.coco_einsum_accumulate, spec, coco.local(lhs), coco.local(rhs), coco.local(acc))
 
     def accumulate(self, acc, part):
         """acc[l] = acc[l] + part[l] in the accumulator's type (one launch: a two-rank sum per local rank)."""
@@ -170,22 +186,22 @@ class CocoCompute:
         n = len(acc)
         ins = [t for pair in zip(acc, part) for t in pair]
         outs = [t for a in acc for t in (a, a)]
-        coco.coco_allreduce(coco.local(ins, ngroups=n), coco.replicated(outs, ngroups=n), self.stream)
+        self._launch(coco.coco_allreduce, coco.local(ins, ngroups=n), coco.replicated(outs, ngroups=n))
 
     def assemble(self, chunks, dim, full):
         """full = the chunks concatenated along ``dim`` in partition order (the AllGather's placement)."""
         self._cuda(list(chunks) + [full])
         n = len(chunks)
-        coco.coco_allgather(coco.sliced(list(chunks), dim), coco.replicated([full] * n), self.stream)
+        self._launch(coco.coco_allgather, coco.sliced(list(chunks), dim), coco.replicated([full] * n))
 
     def fused_slice(self, slices, bias, residual, p, seed, index_base, out):
         """out = dropout(sum over s of slices[s] + bias) + residual on one slice of the flattened tensor,
         whose first element has whole-tensor index ``index_base``."""
         self._cuda(list(slices) + [out] + ([residual] if residual is not None else []))
         n = len(slices)
-        coco.coco_fused_allreduce_at(coco.local(list(slices)), bias,
-                                     None if residual is None else coco.replicated([residual] * n),
-                                     p, seed, index_base, coco.replicated([out] * n), self.stream)
+        self._launch(coco.coco_fused_allreduce_at, coco.local(list(slices)), bias,
+                     None if residual is None else coco.replicated([residual] * n),
+                     p, seed, index_base, coco.replicated([out] * n))
 
 
 # ---------------------------------------------------------- the cost model

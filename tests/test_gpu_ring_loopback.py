@@ -227,3 +227,28 @@ def test_reduce_scatter_ring_schedules(sched, n):
         assert torch.equal(a, b)
         assert np.array_equal(synth.as_f64(a), w)
     assert sorted(trace) == sorted(otrace)
+
+
+@pytest.mark.parametrize("sched", [coco.SCHED_RING, coco.SCHED_UNROLL2])
+def test_compute_on_its_own_stream_is_ordered_with_the_transfers(sched):
+    # The transfers (device copies here, torch.distributed between devices) are ordered on the current
+    # stream; kernels on a side stream are joined to it around every call, so the loop gives the same
+    # bits as on the current stream.
+    n, m, k, nn = 4, 256, 256, 256
+    hl = synth.per_rank(311, 0, n, (n * m, k), torch.bfloat16, "smallint")
+    hr = synth.per_rank(311, 1, n, (k, nn), torch.bfloat16, "smallint")
+    lhs, rhs = _dev(hl), _dev(hr)
+    side = torch.cuda.Stream(device=DEV)
+    outs = []
+    for compute in (ring.CocoCompute(), ring.CocoCompute(stream=side)):
+        out = [torch.full((m, nn), float("nan"), dtype=torch.float32, device=DEV) for _ in range(n)]
+        ring.looped_einsum_reduce_scatter("mk,kn->mn", lhs, rhs, out, ring.LoopbackTransport(n), compute,
+                                          schedule=sched)
+        outs.append(out)
+    torch.cuda.synchronize()
+    coco.coco_device_status()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    want = oracle.looped_einsum_reduce_scatter("mk,kn->mn", _f64(hl), _f64(hr), "m")
+    for o, w in zip(outs[1], want):
+        assert np.array_equal(synth.as_f64(o), w)
