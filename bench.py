@@ -705,7 +705,111 @@ class ScatteredGradients(Workload):
         return self.numel // 4096
 
 
-WORKLOADS = {"c2": MegatronTail, "c2o": MegatronTailOverlap, "c2f": MegatronTailFused, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
+class TinyChain(Workload):
+    """The N=2 fp32 configuration: [Decomp] Fig. 2's MLP (x sliced on the batch, W1 column shards, W2 row
+    shards: the looped AllGather-Einsum, case 1, then the looped Einsum-ReduceScatter) and a
+    FusedAllReduce of two local [4, 16] tensors with bias, dropout p=0.1 and a residual, three calls a
+    step. Each call moves a few kilobytes, so the step is launch-bound and its roofline fraction says
+    nothing about the kernels; the record carries the step replayed from a CUDA graph beside the eager
+    one."""
+
+    name = "tiny_chain"
+    dtype = "f32"
+
+    def __init__(self, dev, n=2, b=8, f=16, h=32, p=0.1, seed=0, cfg=1):
+        from collective_fusedallreduce_gb300 import synth
+        f32 = torch.float32
+        self.n, self.b, self.f, self.hd, self.p, self.seed = n, b, f, h, p, seed
+
+        def uni(tid, shape, rank=None):
+            sd = synth.seed_of(cfg, tid) if rank is None else synth.seed_of(cfg, tid, rank)
+            return synth.tensor(sd, shape, f32, "uniform").to(dev)
+
+        self.x = [uni(0, (b // n, f), r) for r in range(n)]
+        self.w1 = [uni(1, (f, h // n), r) for r in range(n)]
+        self.w2 = [uni(2, (h // n, f), r) for r in range(n)]
+        self.parts = [uni(3, (b // n, f), r) for r in range(n)]
+        self.bias = uni(4, (f,))
+        self.res = uni(5, (b // n, f))
+        self.hbuf = [torch.empty((b, h // n), dtype=f32, device=dev) for _ in range(n)]
+        self.y = [torch.empty((b // n, f), dtype=f32, device=dev) for _ in range(n)]
+        self.out = [torch.empty((b // n, f), dtype=f32, device=dev) for _ in range(n)]
+        self.config = {"workload": "N=2 fp32 chain: Fig. 2 MLP (x[4,16] per rank, W1[16,32] column shards, "
+                                   "W2[32,16] row shards; looped AllGather-Einsum case 1, then looped "
+                                   "Einsum-ReduceScatter) + FusedAllReduce of 2 local [4,16] + bias[16] + dropout "
+                                   "p=0.1 + residual[4,16]; launch-bound (a few KB a call)",
+                       "ranks": n, "l2": "not applicable: a few KB a step, launch-bound",
+                       "inputs": "synthetic U(-1,1)"}
+
+    def kernels(self):
+        n, b, f, hd = self.n, self.b, self.f, self.hd
+        e = 4
+        ag = ((b * f) + n * (f * hd // n) + n * (b * hd // n)) * e  # gathered x read per rank counted once
+        rs = (n * (b * hd // n) + n * (hd // n * f) + n * (b // n * f)) * e
+        far = (n * (b // n * f) * 2 + f + b // n * f) * e
+        return [("k_gemm_simt (looped AllGather-Einsum, case 1)", "hbm", ag, 1),
+                ("k_gemm_simt (looped Einsum-ReduceScatter)", "hbm", rs, 1),
+                ("k_fused_allreduce (2 ranks, bias+dropout+residual)", "hbm", far, 1)]
+
+    def step(self, stream, marks=None):
+        from collective_fusedallreduce_gb300 import coco
+        n = self.n
+        if marks:
+            marks[0].record(stream)
+        coco.coco_looped_ag_einsum("mk,kn->mn", coco.sliced(self.x, 0), coco.local(self.w1), coco.local(self.hbuf),
+                                   stream)
+        if marks:
+            marks[1].record(stream)
+        coco.coco_looped_einsum_rs("mk,kn->mn", coco.sliced(self.hbuf, 1), coco.sliced(self.w2, 0),
+                                   coco.sliced(self.y, 0), stream)
+        if marks:
+            marks[2].record(stream)
+        coco.coco_fused_allreduce(coco.local(self.parts), self.bias, coco.replicated([self.res] * n), self.p,
+                                  self.seed, coco.replicated(self.out), stream)
+        if marks:
+            marks[3].record(stream)
+
+    def graph_seconds(self, stream, steps):
+        """The step captured once into a CUDA graph and replayed ``steps`` times (CUDA events)."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=stream.device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            self.step(side)  # warm the plans outside the capture
+            with torch.cuda.graph(g, stream=side):
+                self.step(side)
+        stream.wait_stream(side)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(torch.cuda.current_stream(stream.device))
+        for _ in range(steps):
+            g.replay()
+        e1.record(torch.cuda.current_stream(stream.device))
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1000.0 / steps
+
+    def host_inputs(self):
+        ins = [(t, t.cpu().pin_memory()) for t in self.x + self.w1 + self.w2 + self.parts + [self.bias, self.res]]
+        return ins, self.out[0]
+
+    def oracle_sample(self, rows):
+        import oracle
+        from collective_fusedallreduce_gb300 import synth
+        x, w1, w2 = ([synth.as_f64(t) for t in ts] for ts in (self.x, self.w1, self.w2))
+        parts = [synth.as_f64(t) for t in self.parts]
+        b, res = synth.as_f64(self.bias), synth.as_f64(self.res)
+        t0 = time.perf_counter()
+        oracle.mlp_1d_forward(x, w1, w2)
+        oracle.fused_allreduce(parts, b, res, self.p, self.seed)
+        return time.perf_counter() - t0, 1.0
+
+    def sample_unit(self):
+        return "steps"
+
+
+WORKLOADS = {"c1": TinyChain, "c2": MegatronTail, "c2o": MegatronTailOverlap, "c2f": MegatronTailFused, "c3": LoopedCase1, "c4a": LoopedCase2, "c4b": LoopedCase3, "c5": Mesh2D,
              "c5b": RsAg, "c5d": AllReduceDirect, "scatter": ScatteredGradients}
 
 
@@ -998,7 +1102,7 @@ def rooflines(key, wl, per_kernel, peaks, clk):
 
 # Every configuration besides the headline, each timed in the same process after it (one GPU's
 # memory at a time: the previous workload's tensors are freed first).
-SUB_CONFIGS = ["c2", "c3", "c4a", "c4b", "c5", "c5b", "c5d", "scatter"]
+SUB_CONFIGS = ["c1", "c2", "c3", "c4a", "c4b", "c5", "c5b", "c5d", "scatter"]
 
 
 def sub_record(key, dev, dist, world, peaks, args, local_rank):
@@ -1026,6 +1130,8 @@ def sub_record(key, dev, dist, world, peaks, args, local_rank):
            "clocks": clk, "gpu_launches": launches}
     if "frac_of_burst" in roof:
         rec["frac_of_burst"] = roof["frac_of_burst"]
+    if hasattr(wl, "graph_seconds"):  # launch-bound: the same step replayed from a CUDA graph
+        rec["graph_ms_per_step"] = wl.graph_seconds(stream, steps) * 1e3
     del wl
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

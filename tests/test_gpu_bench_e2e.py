@@ -17,6 +17,8 @@ def bench():
 
 
 def _device_inputs(name, wl):
+    if name == "c1":
+        return wl.x + wl.w1 + wl.w2 + wl.parts + [wl.bias, wl.res], wl.out[0]
     if name == "c2":
         return wl.inp + wl.w + [wl.bias, wl.res], wl.out[0]
     if name == "c4b":
@@ -24,7 +26,7 @@ def _device_inputs(name, wl):
     return [t for row in wl.grads for t in row], wl.grads[0][0]  # scatter: in place
 
 
-@pytest.mark.parametrize("name", ["c2", "c4b", "scatter"])
+@pytest.mark.parametrize("name", ["c1", "c2", "c4b", "scatter"])
 def test_e2e_restores_the_workload_and_keeps_its_results(bench, name):
     dev = torch.device("cuda", 0)
     wl = bench.WORKLOADS[name](dev)
@@ -47,3 +49,18 @@ def test_e2e_restores_the_workload_and_keeps_its_results(bench, name):
     wl.step(stream)
     torch.cuda.synchronize()
     assert torch.equal(result, ref)
+
+
+def test_tiny_chain_graph_replay_gives_the_eager_bits(bench):
+    # the N=2 fp32 configuration is launch-bound; its record adds the step replayed from a CUDA graph
+    dev = torch.device("cuda", 0)
+    wl = bench.WORKLOADS["c1"](dev)
+    stream = torch.cuda.current_stream(dev)
+    wl.step(stream)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in wl.y + wl.out]
+    for t in wl.y + wl.out:
+        t.fill_(float("nan"))
+    assert wl.graph_seconds(stream, 5) > 0
+    for a, b in zip(wl.y + wl.out, eager):
+        assert torch.equal(a, b)
